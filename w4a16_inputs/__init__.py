@@ -1,0 +1,149 @@
+"""Seeded synthetic inputs for the W4A16 group-quantized linear layer.
+
+This module is shared by the tests, the benchmark and the CPU oracle. It only
+draws random numbers and stores them in the operand dtypes; it holds none of
+the layer's arithmetic (no packing, no dequantisation, no matmul). Both the
+CUDA path and the oracle pack the unpacked 4-bit codes drawn here with their
+own, independent packers.
+
+Value distributions follow the decode and prefill workloads of "Keep W4A16
+zero-points packed at 4 bits instead of expanding to 2 bytes" (§Problem,
+§Results, §Known regression): activations x ~ N(0, 1), 4-bit weight codes and
+zero-points uniform on 0..15, scales uniform on [0.002, 0.02]. The optional
+"signed" scale mode follows the lesson of "qsa_prompt_attn: Q4_0 KV on tensor
+cores" (§What, §Measured "A bug the tests caught"): scales of both signs
+spread over two decades.
+
+Generation order is fixed (x, q, s, z) on one numpy PCG64 stream per seed, so
+a case is reproducible on any host.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+from typing import Optional
+
+import numpy as np
+
+__all__ = [
+    "ACT_DTYPES",
+    "Case",
+    "Workload",
+    "WORKLOADS",
+    "f32_to_act",
+    "make_case",
+    "make_case_for",
+]
+
+ACT_DTYPES = ("f16", "bf16")
+
+
+def _f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
+    """Round float32 values to bfloat16 (nearest, ties to even); return raw uint16 bits."""
+    u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    u = u + (((u >> 16) & 1) + 0x7FFF)
+    return (u >> 16).astype(np.uint16)
+
+
+def f32_to_act(a: np.ndarray, act: str) -> np.ndarray:
+    """Store float32 draws in the activation dtype.
+
+    f16 -> numpy float16 array; bf16 -> numpy uint16 array of bfloat16 bit
+    patterns (numpy has no bfloat16 type).
+    """
+    if act == "f16":
+        return np.ascontiguousarray(a, dtype=np.float32).astype(np.float16)
+    if act == "bf16":
+        return _f32_to_bf16_bits(a)
+    raise ValueError(f"unknown activation dtype {act!r}")
+
+
+@dataclass
+class Case:
+    """One seeded problem, unpacked.
+
+    x  : [M, K] activations in `act` (float16, or uint16 bf16 bit patterns)
+    q  : [K, N] uint8 4-bit weight codes, values 0..15
+    s  : [K/g, N] scales in `act`
+    z  : [K/g, N] uint8 zero-points 0..15, or None for the symmetric layer
+    """
+
+    M: int
+    N: int
+    K: int
+    g: int
+    act: str
+    x: np.ndarray
+    q: np.ndarray
+    s: np.ndarray
+    z: Optional[np.ndarray]
+
+    @property
+    def symmetric(self) -> bool:
+        return self.z is None
+
+
+def make_case(M: int, N: int, K: int, g: int, act: str = "f16", symmetric: bool = False,
+              seed: int = 0, scales: str = "uniform") -> Case:
+    """Draw one case. `scales` is "uniform" (U[0.002, 0.02]) or "signed"
+    (random sign, magnitude log-uniform over [0.002, 0.2])."""
+    if act not in ACT_DTYPES:
+        raise ValueError(f"unknown activation dtype {act!r}")
+    if M < 0 or N < 0 or K < 0 or g <= 0 or K % g:
+        raise ValueError(f"bad shape M={M} N={N} K={K} g={g}")
+    rng = np.random.Generator(np.random.PCG64(seed))
+    x32 = rng.standard_normal((M, K), dtype=np.float32)
+    q = rng.integers(0, 16, size=(K, N), dtype=np.uint8)
+    if scales == "uniform":
+        s32 = (np.float32(0.002) + np.float32(0.018) * rng.random((K // g, N), dtype=np.float32))
+    elif scales == "signed":
+        mag = np.power(10.0, rng.uniform(np.log10(0.002), np.log10(0.2), size=(K // g, N)))
+        sign = np.where(rng.random((K // g, N)) < 0.5, -1.0, 1.0)
+        s32 = (mag * sign).astype(np.float32)
+    else:
+        raise ValueError(f"unknown scale mode {scales!r}")
+    z = None if symmetric else rng.integers(0, 16, size=(K // g, N), dtype=np.uint8)
+    return Case(M=M, N=N, K=K, g=g, act=act, x=f32_to_act(x32, act), q=q,
+                s=f32_to_act(s32, act), z=z)
+
+
+@dataclass(frozen=True)
+class Workload:
+    """A named problem shape. `kernel` is the entry point that serves it."""
+
+    name: str
+    kernel: str  # "gemv" or "gemm"
+    M: int
+    N: int
+    K: int
+    g: int
+    act: str
+    symmetric: bool
+
+    def case(self, seed: int = 0) -> Case:
+        return make_case(self.M, self.N, self.K, self.g, self.act, self.symmetric, seed)
+
+
+def _w(name, kernel, M, N, K, g, act, sym):
+    return Workload(name, kernel, M, N, K, g, act, sym)
+
+
+# The decode and prefill shapes of the W4A16 pages (M x N x K, group g).
+WORKLOADS = {w.name: w for w in [
+    # small square decode GEMV, g=128, fp16, asymmetric
+    _w("gemv_1x2048x2048_g128_f16_asym", "gemv", 1, 2048, 2048, 128, "f16", False),
+    # gate_up-like decode GEMV (~116 MB of int4 weights), g=32, fp16, asymmetric
+    _w("gemv_1x43008x5376_g32_f16_asym", "gemv", 1, 43008, 5376, 32, "f16", False),
+    # batch-4 g=128 asymmetric sweep, fp16 and bf16
+    *[_w(f"gemv_4x{N}x{K}_g128_{a}_asym", "gemv", 4, N, K, 128, a, False)
+      for a in ("f16", "bf16")
+      for (N, K) in ((2048, 2048), (2048, 2560), (6144, 2048), (4096, 2048))],
+    # qkv-like and down-like decode GEMV, g=32, bf16, symmetric and asymmetric
+    *[_w(f"gemv_1x{N}x{K}_g32_bf16_{'sym' if s else 'asym'}", "gemv", 1, N, K, 32, "bf16", s)
+      for (N, K) in ((16384, 5376), (5376, 21504)) for s in (True, False)],
+    # prefill GEMM on the gate_up shape, g=32, bf16 in/out
+    _w("gemm_2048x43008x5376_g32_bf16_asym", "gemm", 2048, 43008, 5376, 32, "bf16", False),
+]}
+
+
+def make_case_for(name: str, seed: int = 0) -> Case:
+    return WORKLOADS[name].case(seed)

@@ -1,0 +1,54 @@
+"""Algorithmic byte and FLOP counts of one W4A16 layer call.
+
+The byte count is what the layer must move at minimum: packed 4-bit weights,
+one scale per (group, column), packed 4-bit zero-points, the activations and
+the output. This is the convention of "Keep W4A16 zero-points packed at 4 bits
+instead of expanding to 2 bytes" (§Problem: weights + scale + zero-point
+bytes streamed per call), extended by the x and y bytes. Expanded zero-points
+(one activation-dtype value per group and column, the layout that page
+replaces) are counted only by `expanded_zero_bytes`, never in the roofline.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+ACT_BYTES = {"f16": 2, "bf16": 2}
+
+
+@dataclass(frozen=True)
+class LayerBytes:
+    weights: int
+    scales: int
+    zeros: int
+    x: int
+    y: int
+
+    @property
+    def operands(self) -> int:
+        """weights + scales + packed zero-points (what the decode kernel streams)."""
+        return self.weights + self.scales + self.zeros
+
+    @property
+    def total(self) -> int:
+        return self.operands + self.x + self.y
+
+
+def layer_bytes(M: int, N: int, K: int, g: int, symmetric: bool = False, act: str = "f16") -> LayerBytes:
+    a = ACT_BYTES[act]
+    groups = K // g
+    return LayerBytes(
+        weights=K * N // 2,
+        scales=groups * N * a,
+        zeros=0 if symmetric else groups * N // 2,
+        x=M * K * a,
+        y=M * N * a,
+    )
+
+
+def expanded_zero_bytes(N: int, K: int, g: int, act: str = "f16") -> int:
+    """Bytes of zero-points stored one activation-dtype value per (group, column)."""
+    return (K // g) * N * ACT_BYTES[act]
+
+
+def layer_flops(M: int, N: int, K: int) -> int:
+    return 2 * M * N * K
