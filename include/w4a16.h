@@ -1,0 +1,188 @@
+/*
+ * w4a16.h -- C ABI of libw4a16, the W4A16 group-quantized linear layer for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The layer (one weight-only int4 linear layer, activations in fp16/bf16):
+ *
+ *     y[m, n] = sum_k x[m, k] * (q[k, n] - z[k / g, n]) * s[k / g, n]
+ *
+ *   x   [M, K]    activations, fp16 or bf16, row-major
+ *   q   [K, N]    4-bit weight codes 0..15, stored packed (see qweight)
+ *   s   [K/g, N]  one scale per group of g rows of K and per column, same
+ *                 dtype as x
+ *   z   [K/g, N]  4-bit zero-points 0..15, stored packed (see qzeros); the
+ *                 symmetric layer has no zero-point tensor and uses z = 8,
+ *                 the "code - 8" recentring described on "qsa_prompt_attn:
+ *                 Q4_0 KV on tensor cores" (section "What")
+ *   y   [M, N]    output, same dtype as x, rounded to nearest-even from an
+ *                 FP32 accumulator
+ *
+ * Packed layouts (words are read as uint32 bit patterns):
+ *   qweight int32 [K/8, N]    nibble j (bits 4j..4j+3) of word [w, n] holds
+ *                             q[8w + j, n]
+ *   qzeros  int32 [K/g, N/8]  the zero-point of column n sits in word
+ *                             [t, n/8] at bits 4*(n%8). This is the packed
+ *                             zero-point layout of "Keep W4A16 zero-points
+ *                             packed at 4 bits instead of expanding to 2
+ *                             bytes" (section "Change"); that page's point is
+ *                             that the kernel reads zero-points in this form,
+ *                             0.5 byte per group and column, and never an
+ *                             expanded activation-dtype copy of them.
+ *
+ * Conventions for every entry point below:
+ *   - Every tensor pointer is a DEVICE pointer owned by the caller; tensors
+ *     are dense and row-major. The library never allocates, frees or
+ *     synchronises device memory, except w4a16_device_status, which
+ *     synchronises the given stream.
+ *   - Calls are asynchronous on `stream` (NULL = the legacy default stream).
+ *   - All argument checks run on the host BEFORE anything is launched; a
+ *     failed check returns an error status and launches nothing.
+ *   - A launch error is returned as W4A16_ERR_CUDA. The library does not
+ *     clear CUDA's sticky error state.
+ *   - The library runs only on compute capability 10.3 (GB300); any other
+ *     device gives W4A16_ERR_DEVICE.
+ *   - Shape limits: N % 8 == 0, K % g == 0, g in {32, 64, 128, 256}, all
+ *     dimensions > 0 and < 2^31, base pointers 16-byte aligned.
+ */
+#ifndef W4A16_H
+#define W4A16_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define W4A16_ABI_VERSION 1
+
+typedef enum {
+    W4A16_OK = 0,
+    W4A16_ERR_NULL = 1,        /* a required pointer is NULL                          */
+    W4A16_ERR_SHAPE = 2,       /* a dimension is out of range or inconsistent         */
+    W4A16_ERR_DTYPE = 3,       /* unknown activation dtype                            */
+    W4A16_ERR_ALIGN = 4,       /* a base pointer is not 16-byte aligned               */
+    W4A16_ERR_UNSUPPORTED = 5, /* valid request this build does not implement         */
+    W4A16_ERR_DEVICE = 6,      /* no CUDA device, or not compute capability 10.3      */
+    W4A16_ERR_WORKSPACE = 7,   /* workspace missing or smaller than required          */
+    W4A16_ERR_CUDA = 8,        /* a CUDA runtime call or a launch failed              */
+    W4A16_ERR_TIMEOUT = 9      /* a device-side pipeline wait ran out (see below)     */
+} w4a16_status;
+
+typedef enum {
+    W4A16_F16 = 0,
+    W4A16_BF16 = 1
+} w4a16_dtype;
+
+/* Same type as cudaStream_t; declared here so the header needs no CUDA include. */
+typedef struct CUstream_st* w4a16_stream;
+
+/* Which kernel a workspace query is for. */
+typedef enum {
+    W4A16_OP_GEMV = 0,
+    W4A16_OP_GEMM = 1
+} w4a16_op;
+
+/*
+ * w4a16_pack -- pack 4-bit codes eight to a 32-bit word.
+ *
+ * src  uint8 [rows, cols]; only the low 4 bits of each byte are used.
+ * dim  0: pack along rows -> dst int32 [rows/8, cols]; nibble j of word
+ *         [w, c] is src[8w + j, c] (the qweight layout, rows = K);
+ *      1: pack along cols -> dst int32 [rows, cols/8]; column c goes to word
+ *         [r, c/8] at bits 4*(c%8) (the qzeros layout of "Keep W4A16
+ *         zero-points packed at 4 bits instead of expanding to 2 bytes",
+ *         section "Change", rows = K/g, cols = N).
+ * The packed dimension must be a multiple of 8. Bit-exact; deterministic.
+ * Errors: NULL, SHAPE (non-positive or not a multiple of 8), ALIGN (either
+ * pointer not 16-byte aligned), DEVICE, CUDA.
+ */
+w4a16_status w4a16_pack(const uint8_t* src, int32_t* dst, int64_t rows, int64_t cols, int dim,
+                        w4a16_stream stream);
+
+/*
+ * w4a16_unpack -- inverse of w4a16_pack. `rows`, `cols` and `dim` describe the
+ * UNPACKED tensor dst uint8 [rows, cols] (values 0..15); src is the packed
+ * int32 tensor of w4a16_pack's output shape. This is the inverse that the
+ * zero-point page names as unpacking along the packed dimension. Errors as
+ * for w4a16_pack.
+ */
+w4a16_status w4a16_unpack(const int32_t* src, uint8_t* dst, int64_t rows, int64_t cols, int dim,
+                          w4a16_stream stream);
+
+/*
+ * w4a16_workspace_bytes -- device workspace the op needs for this shape on
+ * the current device (0 if none). The GEMV and the GEMM of this build need
+ * none; the argument exists so a caller can size a workspace without knowing
+ * which kernel variant runs. Returns 0 for invalid shapes.
+ */
+size_t w4a16_workspace_bytes(w4a16_op op, int64_t M, int64_t N, int64_t K, int64_t g);
+
+/*
+ * w4a16_gemv -- decode path, 1 <= M <= 16.
+ *
+ * Streams qweight, scales and qzeros once with 128-bit coalesced loads, splits
+ * K across the warps of a thread-block cluster and reduces the partial sums
+ * through shared and distributed shared memory in a fixed order (the result
+ * is deterministic). This is the memory-bound skinny kernel that the
+ * zero-point page measures ("Results" and "Known regression").
+ *
+ * x        [M, K] dtype `dt`
+ * qweight  int32 [K/8, N]
+ * scales   [K/g, N] dtype `dt`
+ * qzeros   int32 [K/g, N/8], or NULL for the symmetric layer (z = 8)
+ * y        [M, N] dtype `dt`, written (not accumulated into)
+ * workspace, workspace_bytes   unused by this build; may be NULL / 0
+ * Errors: NULL, SHAPE (M outside 1..16, N % 8, K % g), UNSUPPORTED (g not in
+ * {32, 64, 128, 256}), DTYPE, ALIGN, WORKSPACE, DEVICE, CUDA.
+ */
+w4a16_status w4a16_gemv(const void* x, const int32_t* qweight, const void* scales,
+                        const int32_t* qzeros, void* y, int64_t M, int64_t N, int64_t K,
+                        int64_t g, w4a16_dtype dt, void* workspace, size_t workspace_bytes,
+                        w4a16_stream stream);
+
+/*
+ * w4a16_gemm -- prefill path, any M >= 1 (built for M in the hundreds or
+ * more; small M works but wastes most of a 128-row tile).
+ *
+ * Each CTA of a persistent grid owns 128 x 256 output tiles. Per 64-deep
+ * K step, TMA brings the x tile and the packed weight tile into shared
+ * memory, eight warps dequantise the weight tile ONCE into a shared bf16/fp16
+ * operand tile that the whole tile's MMAs consume (the cooperative shared
+ * tile of "ROCm KQuantGemmKWmmaQ4K/Q6K: redesign around a cooperative shared
+ * tile", section "Confirmed mechanism"), and one thread issues tcgen05.mma
+ * with the FP32 accumulator in tensor memory. M and N tails are handled by
+ * TMA zero fill on loads and predicated stores. The dequantised weight is
+ * (q - z) * s rounded once to the activation dtype.
+ *
+ * Arguments and errors as w4a16_gemv, except M >= 1 with no upper limit.
+ * W4A16_ERR_TIMEOUT is never returned here; a pipeline wait that runs out
+ * sets a device flag that w4a16_device_status reports.
+ */
+w4a16_status w4a16_gemm(const void* x, const int32_t* qweight, const void* scales,
+                        const int32_t* qzeros, void* y, int64_t M, int64_t N, int64_t K,
+                        int64_t g, w4a16_dtype dt, void* workspace, size_t workspace_bytes,
+                        w4a16_stream stream);
+
+/*
+ * w4a16_device_status -- synchronise `stream`, then read and clear the
+ * device-side error word of the current device. Every wait on an mbarrier
+ * inside the GEMM pipeline gives up after about two seconds; the kernel then
+ * records W4A16_ERR_TIMEOUT there, drains its own copies in flight, frees its
+ * tensor memory and returns, so the CUDA context stays usable. Returns
+ * W4A16_OK when nothing was recorded, W4A16_ERR_CUDA if synchronisation
+ * failed.
+ */
+w4a16_status w4a16_device_status(w4a16_stream stream);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char* w4a16_status_string(w4a16_status status);
+
+/* W4A16_ABI_VERSION of the compiled library. */
+int w4a16_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W4A16_H */

@@ -1,0 +1,160 @@
+"""GPU parity of w4a16_gemv and w4a16_gemm against the FP64 oracle on small
+shapes that span several tiles and ragged tails, plus bit-exact special cases,
+determinism, guard bands around the output and host-side rejections."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import weight_only_int4_gb300 as w4  # noqa: E402
+from gpu_util import (TORCH_DTYPE, DeviceCase, act_to_torch, assert_within_tol, check_guards,  # noqa: E402
+                      guarded_out, torch_to_f64)
+from oracle import w4a16_oracle as O  # noqa: E402
+from w4a16_inputs import make_case  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+OPS = {"gemv": w4.gemv, "gemm": w4.gemm}
+
+
+def run(op, dc, out=None):
+    return OPS[op](dc.x, dc.qw, dc.s, dc.qz, dc.g, out=out)
+
+
+def parity(op, M, N, K, g, act, sym, scales="uniform", seed=0):
+    dc = DeviceCase(make_case(M, N, K, g, act, sym, seed=seed, scales=scales))
+    buf, y, pad = guarded_out(M, N, TORCH_DTYPE[act])
+    run(op, dc, out=y)
+    torch.cuda.synchronize()
+    check_guards(buf, pad)
+    assert_within_tol(y, dc.reference(), act, f"{op} M={M} N={N} K={K} g={g} {act} sym={sym}")
+    assert w4.device_status() == w4.OK
+
+
+GEMV_SHAPES = [(8, 64), (264, 256), (776, 1024), (2048, 384)]
+
+
+@pytest.mark.parametrize("act", ["f16", "bf16"])
+@pytest.mark.parametrize("g", [32, 128])
+@pytest.mark.parametrize("sym", [False, True])
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 7, 8, 16])
+def test_gemv_parity(act, g, sym, M):
+    for (N, K) in GEMV_SHAPES:
+        if K % g:
+            K = g * max(1, K // g)
+        parity("gemv", M, N, K, g, act, sym, seed=M + N + K)
+
+
+@pytest.mark.parametrize("g", [64, 256])
+@pytest.mark.parametrize("M", [1, 5, 11])
+def test_gemv_other_groups(g, M):
+    parity("gemv", M, 520, 2 * g * 3, g, "bf16", False, seed=g + M)
+    parity("gemv", M, 520, 2 * g * 3, g, "f16", True, seed=g + M + 1)
+
+
+@pytest.mark.parametrize("act", ["f16", "bf16"])
+@pytest.mark.parametrize("M", [1, 4])
+def test_gemv_signed_scales(act, M):
+    parity("gemv", M, 776, 1024, 32, act, False, scales="signed", seed=3)
+
+
+GEMM_SHAPES = [(256, 256), (520, 384), (8, 128), (1032, 640)]
+
+
+@pytest.mark.parametrize("act", ["bf16", "f16"])
+@pytest.mark.parametrize("g", [32, 128])
+@pytest.mark.parametrize("sym", [False, True])
+@pytest.mark.parametrize("M", [1, 17, 128, 255, 256, 300])
+def test_gemm_parity(act, g, sym, M):
+    for (N, K) in GEMM_SHAPES:
+        if K % g:
+            K = g * max(1, K // g)
+        parity("gemm", M, N, K, g, act, sym, seed=M + N + K)
+
+
+@pytest.mark.parametrize("g", [64, 256])
+def test_gemm_other_groups(g):
+    parity("gemm", 200, 520, 2 * g * 3, g, "bf16", False, seed=g)
+
+
+@pytest.mark.parametrize("act", ["bf16", "f16"])
+def test_gemm_signed_scales(act):
+    parity("gemm", 384, 776, 1024, 32, act, False, scales="signed", seed=5)
+
+
+def test_gemm_k_tail_half_step():
+    # K = 96 with g = 32: the last 64-deep step is half outside K
+    parity("gemm", 130, 264, 96, 32, "bf16", False, seed=1)
+    parity("gemm", 130, 264, 160, 32, "f16", True, seed=2)
+
+
+def test_gemm_many_tiles_multiple_waves():
+    # more tiles than SMs: every CTA loops over several tiles and both accumulators
+    parity("gemm", 1024, 8192, 256, 128, "bf16", False, seed=9)
+
+
+@pytest.mark.parametrize("op", ["gemv", "gemm"])
+@pytest.mark.parametrize("act", ["f16", "bf16"])
+@pytest.mark.parametrize("sym", [False, True])
+def test_onehot_bit_exact(op, act, sym):
+    """x = e_k selects one dequantised weight row: y = RN((q - z) * s), bit for bit."""
+    M, N, K, g = (5 if op == "gemv" else 130), 264, 256, 32
+    case = make_case(M, N, K, g, act, sym, seed=17)
+    ks = [(37 * m + 5) % K for m in range(M)]
+    x = np.zeros((M, K), dtype=np.float32)
+    for m, k in enumerate(ks):
+        x[m, k] = 1.0
+    case.x = x.astype(np.float16) if act == "f16" else (x.view(np.uint32) >> 16).astype(np.uint16)
+    dc = DeviceCase(case)
+    y = torch_to_f64(run(op, dc))
+    s = O.widen(case.s, act)
+    for m, k in enumerate(ks):
+        z = 8 if sym else case.z[k // g].astype(np.int64)
+        want = O.round_to_act((case.q[k].astype(np.int64) - z) * s[k // g], act)
+        assert np.array_equal(y[m], want), (op, act, sym, m)
+
+
+@pytest.mark.parametrize("op", ["gemv", "gemm"])
+@pytest.mark.parametrize("act", ["f16", "bf16"])
+def test_q_equals_z_is_exactly_zero(op, act):
+    M = 3 if op == "gemv" else 200
+    case = make_case(M, 264, 256, 32, act, False, seed=23)
+    case.q = np.repeat(case.z, 32, axis=0)
+    y = run(op, DeviceCase(case))
+    assert torch.count_nonzero(y).item() == 0
+
+
+@pytest.mark.parametrize("op,M", [("gemv", 4), ("gemm", 300)])
+def test_deterministic(op, M):
+    dc = DeviceCase(make_case(M, 2056, 2048, 128, "bf16", False, seed=31))
+    a = run(op, dc).clone()
+    b = run(op, dc).clone()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_gemv_and_gemm_agree():
+    dc = DeviceCase(make_case(16, 776, 1024, 32, "bf16", False, seed=41))
+    a = torch_to_f64(w4.gemv(dc.x, dc.qw, dc.s, dc.qz, 32))
+    b = torch_to_f64(w4.gemm(dc.x, dc.qw, dc.s, dc.qz, 32))
+    ref = dc.reference()
+    assert np.abs(a - b).max() <= 2 * 1.6e-2 * np.abs(ref).max()
+
+
+def test_binding_rejections():
+    dc = DeviceCase(make_case(2, 64, 128, 32, "f16", False, seed=0))
+    z_act = torch.zeros(4, 64, dtype=torch.float16, device="cuda")
+    with pytest.raises(TypeError):
+        w4.gemv(dc.x, dc.qw, dc.s, z_act, 32)                       # zero-points in the activation dtype
+    with pytest.raises(TypeError):
+        w4.gemv(dc.x, dc.qw, dc.s.to(torch.bfloat16), dc.qz, 32)   # scales dtype differs from x
+    with pytest.raises(ValueError):
+        w4.gemv(dc.x, dc.qw, dc.s, dc.qz, 64)                       # scales shape vs g
+    big = torch.zeros(2 * 128 + 8, dtype=torch.float16, device="cuda")
+    x_mis = big[1:1 + 256].view(2, 128)                               # 2-byte offset: not 16-byte aligned
+    with pytest.raises(w4.W4A16Error) as e:
+        w4.gemv(x_mis, dc.qw, dc.s, dc.qz, 32)
+    assert e.value.status == w4.ERR_ALIGN
+    x17 = act_to_torch(make_case(17, 64, 128, 32, "f16", False).x, "f16")
+    with pytest.raises(w4.W4A16Error) as e:
+        w4.gemv(x17, dc.qw, dc.s, dc.qz, 32)
+    assert e.value.status == w4.ERR_SHAPE

@@ -1,0 +1,173 @@
+// C ABI of libw4a16: argument validation, device gate, dispatch.
+// Declarations and the contract of every entry point are in include/w4a16.h.
+#include "w4a16.h"
+
+#include "internal.h"
+
+#include <mutex>
+
+namespace w4a16 {
+
+cudaError_t current_device_props(DeviceProps* out) {
+    static std::mutex mu;
+    static DeviceProps cache[64];
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[dev].device != dev) {
+        DeviceProps p;
+        p.device = dev;
+        if ((e = cudaDeviceGetAttribute(&p.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+        if ((e = cudaDeviceGetAttribute(&p.cc_major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess) return e;
+        if ((e = cudaDeviceGetAttribute(&p.cc_minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess) return e;
+        int optin = 0;
+        if ((e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess) return e;
+        p.smem_optin = static_cast<size_t>(optin);
+        cache[dev] = p;
+    }
+    *out = cache[dev];
+    return cudaSuccess;
+}
+
+}  // namespace w4a16
+
+namespace {
+
+using w4a16::DeviceProps;
+
+constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool supported_group(int64_t g) { return g == 32 || g == 64 || g == 128 || g == 256; }
+
+// Device gate: a CUDA device must be current and be compute capability 10.3.
+w4a16_status device_gate(DeviceProps* dp) {
+    if (w4a16::current_device_props(dp) != cudaSuccess) {
+        cudaGetLastError();   // the failed query is not the caller's error
+        return W4A16_ERR_DEVICE;
+    }
+    if (dp->cc_major != 10 || dp->cc_minor != 3) return W4A16_ERR_DEVICE;
+    return W4A16_OK;
+}
+
+w4a16_status check_pack_args(const void* src, const void* dst, int64_t rows, int64_t cols, int dim) {
+    if (!src || !dst) return W4A16_ERR_NULL;
+    if (dim != 0 && dim != 1) return W4A16_ERR_SHAPE;
+    if (rows <= 0 || cols <= 0 || rows > kMaxDim || cols > kMaxDim) return W4A16_ERR_SHAPE;
+    if ((dim == 0 ? rows : cols) % 8 != 0) return W4A16_ERR_SHAPE;
+    if (!aligned16(src) || !aligned16(dst)) return W4A16_ERR_ALIGN;
+    return W4A16_OK;
+}
+
+w4a16_status check_layer_args(const void* x, const int32_t* qweight, const void* scales, const int32_t* qzeros,
+                              const void* y, int64_t M, int64_t N, int64_t K, int64_t g, w4a16_dtype dt,
+                              int64_t max_m) {
+    if (!x || !qweight || !scales || !y) return W4A16_ERR_NULL;
+    if (dt != W4A16_F16 && dt != W4A16_BF16) return W4A16_ERR_DTYPE;
+    if (M < 1 || N < 1 || K < 1 || g < 1) return W4A16_ERR_SHAPE;
+    if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return W4A16_ERR_SHAPE;
+    if (max_m > 0 && M > max_m) return W4A16_ERR_SHAPE;
+    if (N % 8 != 0 || K % g != 0) return W4A16_ERR_SHAPE;
+    if (!supported_group(g)) return W4A16_ERR_UNSUPPORTED;
+    if (!aligned16(x) || !aligned16(qweight) || !aligned16(scales) || !aligned16(y) ||
+        (qzeros && !aligned16(qzeros)))
+        return W4A16_ERR_ALIGN;
+    return W4A16_OK;
+}
+
+w4a16_status from_cuda(cudaError_t e) { return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+int w4a16_abi_version(void) { return W4A16_ABI_VERSION; }
+
+const char* w4a16_status_string(w4a16_status status) {
+    switch (status) {
+        case W4A16_OK: return "W4A16_OK";
+        case W4A16_ERR_NULL: return "W4A16_ERR_NULL";
+        case W4A16_ERR_SHAPE: return "W4A16_ERR_SHAPE";
+        case W4A16_ERR_DTYPE: return "W4A16_ERR_DTYPE";
+        case W4A16_ERR_ALIGN: return "W4A16_ERR_ALIGN";
+        case W4A16_ERR_UNSUPPORTED: return "W4A16_ERR_UNSUPPORTED";
+        case W4A16_ERR_DEVICE: return "W4A16_ERR_DEVICE";
+        case W4A16_ERR_WORKSPACE: return "W4A16_ERR_WORKSPACE";
+        case W4A16_ERR_CUDA: return "W4A16_ERR_CUDA";
+        case W4A16_ERR_TIMEOUT: return "W4A16_ERR_TIMEOUT";
+    }
+    return "W4A16_ERR_UNKNOWN";
+}
+
+w4a16_status w4a16_pack(const uint8_t* src, int32_t* dst, int64_t rows, int64_t cols, int dim,
+                        w4a16_stream stream) {
+    w4a16_status st = check_pack_args(src, dst, rows, cols, dim);
+    if (st != W4A16_OK) return st;
+    DeviceProps dp;
+    if ((st = device_gate(&dp)) != W4A16_OK) return st;
+    return from_cuda(w4a16::launch_pack(src, reinterpret_cast<uint32_t*>(dst), rows, cols, dim, dp,
+                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
+w4a16_status w4a16_unpack(const int32_t* src, uint8_t* dst, int64_t rows, int64_t cols, int dim,
+                          w4a16_stream stream) {
+    w4a16_status st = check_pack_args(src, dst, rows, cols, dim);
+    if (st != W4A16_OK) return st;
+    DeviceProps dp;
+    if ((st = device_gate(&dp)) != W4A16_OK) return st;
+    return from_cuda(w4a16::launch_unpack(reinterpret_cast<const uint32_t*>(src), dst, rows, cols, dim, dp,
+                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t w4a16_workspace_bytes(w4a16_op op, int64_t M, int64_t N, int64_t K, int64_t g) {
+    (void)op;
+    (void)M;
+    (void)N;
+    (void)K;
+    (void)g;
+    return 0;
+}
+
+w4a16_status w4a16_gemv(const void* x, const int32_t* qweight, const void* scales, const int32_t* qzeros, void* y,
+                        int64_t M, int64_t N, int64_t K, int64_t g, w4a16_dtype dt, void* workspace,
+                        size_t workspace_bytes, w4a16_stream stream) {
+    (void)workspace;
+    (void)workspace_bytes;
+    w4a16_status st = check_layer_args(x, qweight, scales, qzeros, y, M, N, K, g, dt, 16);
+    if (st != W4A16_OK) return st;
+    DeviceProps dp;
+    if ((st = device_gate(&dp)) != W4A16_OK) return st;
+    const w4a16::GemvPlan plan = w4a16::plan_gemv((int)M, (int)N, (int)K, (int)g, dp);
+    return from_cuda(w4a16::launch_gemv(x, reinterpret_cast<const uint32_t*>(qweight), scales,
+                                        reinterpret_cast<const uint32_t*>(qzeros), y, (int)M, (int)N, (int)K, (int)g,
+                                        dt == W4A16_BF16, plan, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+w4a16_status w4a16_gemm(const void* x, const int32_t* qweight, const void* scales, const int32_t* qzeros, void* y,
+                        int64_t M, int64_t N, int64_t K, int64_t g, w4a16_dtype dt, void* workspace,
+                        size_t workspace_bytes, w4a16_stream stream) {
+    (void)workspace;
+    (void)workspace_bytes;
+    w4a16_status st = check_layer_args(x, qweight, scales, qzeros, y, M, N, K, g, dt, 0);
+    if (st != W4A16_OK) return st;
+    DeviceProps dp;
+    if ((st = device_gate(&dp)) != W4A16_OK) return st;
+    return from_cuda(w4a16::launch_gemm(x, reinterpret_cast<const uint32_t*>(qweight), scales,
+                                        reinterpret_cast<const uint32_t*>(qzeros), y, (int)M, (int)N, (int)K, (int)g,
+                                        dt == W4A16_BF16, dp, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+w4a16_status w4a16_device_status(w4a16_stream stream) {
+    DeviceProps dp;
+    w4a16_status st = device_gate(&dp);
+    if (st != W4A16_OK) return st;
+    uint32_t v = 0;
+    if (w4a16::read_and_clear_device_error(&v, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return W4A16_ERR_CUDA;
+    return v ? W4A16_ERR_TIMEOUT : W4A16_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,439 @@
+// Prefill GEMM of the W4A16 layer on the 5th-generation tensor cores.
+//
+// Design (one CTA per SM, persistent over 128 x 256 output tiles):
+//
+//   warp 0      TMA producer: per 64-deep K step, the x tile [128 x 64]
+//               (128-byte swizzle) and the packed weight tile [8 words x 256]
+//               land in one stage of a shared-memory ring.
+//   warps 8-15  dequantise the packed tile ONCE into a [256 x 64] fp16/bf16
+//               operand tile in the canonical K-major 128-byte-swizzled layout
+//               the MMA reads: w = (q - z) * s, with (q - z) exact in 16-bit
+//               arithmetic and one rounding for the product. This is the
+//               cooperative shared tile of "ROCm KQuantGemmKWmmaQ4K/Q6K:
+//               redesign around a cooperative shared tile" (section "Confirmed
+//               mechanism"): the weight tile is loaded and dequantised once per
+//               CTA and every MMA of the tile consumes the same copy. As on
+//               "Add BF16xFP4 MoE GEMM stage1 kernel" (section "Technical
+//               Details"), weights are decoded in software before the MMA,
+//               which takes fp16/bf16 operands.
+//   warp 1      one thread issues tcgen05.mma (kind::f16, M=128, N=256, K=16)
+//               into an FP32 accumulator in tensor memory; two accumulators
+//               alternate so the epilogue of one tile overlaps the next.
+//   warps 4-7   epilogue: tcgen05.ld from tensor memory, round to the output
+//               dtype, predicated 16-byte stores (every store is guarded on
+//               both M and N, the lesson of the col_n_valid guard on the MoE
+//               page, section "Technical Details").
+//
+// Every mbarrier wait is bounded (about two seconds); on expiry the kernel
+// records W4A16_ERR_TIMEOUT in a device word, every role stops, the producer
+// and the MMA thread wait (bounded) for their own operations in flight, tensor
+// memory is freed and the kernel returns.
+#include "internal.h"
+#include "ptx.cuh"
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+
+namespace w4a16 {
+
+__device__ unsigned int g_device_error = 0;
+
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64;
+constexpr int kStages = 3;
+constexpr int kThreads = 512;
+constexpr int kEpiWarp0 = 4;             // warps 4..7
+constexpr int kDeqWarp0 = 8;             // warps 8..15
+constexpr int kDeqThreads = 256;         // one dequant thread per column of the tile
+constexpr uint32_t kABytes = BM * BK * 2;            // 16 KB
+constexpr uint32_t kBBytes = BN * BK * 2;            // 32 KB
+constexpr uint32_t kWBytes = (BK / 8) * BN * 4;      //  8 KB
+constexpr uint32_t kStageBytes = kABytes + kBBytes + kWBytes;
+constexpr uint32_t kTmemCols = 2 * BN;               // two accumulators
+constexpr unsigned long long kWaitLimitCycles = 4000000000ull;   // ~2 s at 2 GHz
+constexpr unsigned int kErrTimeout = 9u;
+
+struct __align__(8) Barriers {
+    uint64_t full[kStages];     // TMA bytes landed (x tile + packed weight tile)
+    uint64_t bfull[kStages];    // dequantised operand tile written (256 arrivals)
+    uint64_t empty[kStages];    // MMAs reading the stage retired (tcgen05.commit)
+    uint64_t tfull[2];          // accumulator complete
+    uint64_t tempty[2];         // accumulator drained by the epilogue (128 arrivals)
+    uint64_t drain;             // final commit of the MMA thread
+    uint32_t tmem_base;
+    int abort;
+};
+
+constexpr size_t kSmemBytes = 1024 /*align slack*/ + kStages * kStageBytes + sizeof(Barriers);
+
+// Bounded wait: false if the wait ran out (or another role already gave up).
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = clock64();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 15u) == 0) {
+            if (*abort) return false;
+            if (clock64() - t0 > kWaitLimitCycles) {
+                *abort = 1;
+                atomicOr(&g_device_error, 1u << kErrTimeout);
+                return false;
+            }
+        }
+    }
+}
+
+template <bool kBf16>
+struct Deq;
+template <>
+struct Deq<false> {
+    static constexpr uint32_t kMagic = 0x64006400u;   // fp16 1024.0
+    __device__ static uint32_t sub2(uint32_t a, uint32_t b) {
+        uint32_t d;
+        asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+        return d;
+    }
+    __device__ static uint32_t mul2(uint32_t a, uint32_t b) {
+        uint32_t d;
+        asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+        return d;
+    }
+    __device__ static uint32_t pack2(float lo, float hi) {
+        const __half2 h = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<const uint32_t*>(&h);
+    }
+};
+template <>
+struct Deq<true> {
+    static constexpr uint32_t kMagic = 0x43004300u;   // bf16 128.0
+    __device__ static uint32_t sub2(uint32_t a, uint32_t b) {
+        uint32_t d;
+        asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+        return d;
+    }
+    __device__ static uint32_t mul2(uint32_t a, uint32_t b) {
+        uint32_t d;
+        asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+        return d;
+    }
+    __device__ static uint32_t pack2(float lo, float hi) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<const uint32_t*>(&h);
+    }
+};
+
+template <bool kBf16, bool kSym>
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
+            const uint16_t* __restrict__ sc, const uint32_t* __restrict__ qz, uint16_t* __restrict__ y, int M,
+            int N, int K, int g) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Barriers* bars = reinterpret_cast<Barriers*>(smem + kStages * kStageBytes);
+    const uint32_t smem_base = smem_u32(smem);
+    auto stage_a = [&](int s) { return smem_base + s * kStageBytes; };
+    auto stage_b = [&](int s) { return smem_base + s * kStageBytes + kABytes; };
+    auto stage_w = [&](int s) { return smem + s * kStageBytes + kABytes + kBBytes; };
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int num_m = (M + BM - 1) / BM, num_n = (N + BN - 1) / BN;
+    const int tiles = num_m * num_n;
+    const int kt_total = (K + BK - 1) / BK;
+    volatile int* abort_flag = &bars->abort;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(smem_u32(&bars->full[s]), 1);
+            mbar_init(smem_u32(&bars->bfull[s]), kDeqThreads);
+            mbar_init(smem_u32(&bars->empty[s]), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(smem_u32(&bars->tfull[a]), 1);
+            mbar_init(smem_u32(&bars->tempty[a]), 128);
+        }
+        mbar_init(smem_u32(&bars->drain), 1);
+        bars->abort = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmap_x);
+        tma_prefetch_desc(&tmap_w);
+    }
+    if (warp == 2) tmem_alloc(smem_u32(&bars->tmem_base), kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = bars->tmem_base;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t issued_parity[kStages];
+            bool issued[kStages];
+            for (int s = 0; s < kStages; ++s) issued[s] = false, issued_parity[s] = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+                const int m_blk = t % num_m, n_blk = t / num_m;
+                for (int kt = 0; kt < kt_total; ++kt) {
+                    if (!wait_bar(smem_u32(&bars->empty[stage]), phase ^ 1u, abort_flag)) { ok = false; break; }
+                    const uint32_t fb = smem_u32(&bars->full[stage]);
+                    mbar_arrive_expect_tx(fb, kABytes + kWBytes);
+                    tma_load_2d(stage_a(stage), &tmap_x, kt * BK, m_blk * BM, fb);
+                    tma_load_2d(smem_u32(stage_w(stage)), &tmap_w, n_blk * BN, kt * (BK / 8), fb);
+                    issued[stage] = true;
+                    issued_parity[stage] = phase;
+                    if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                }
+            }
+            // copies still in flight must land before this CTA's shared memory is released
+            for (int s = 0; s < kStages; ++s) {
+                if (!issued[s]) continue;
+                const uint32_t fb = smem_u32(&bars->full[s]);
+                const unsigned long long t0 = clock64();
+                while (!mbar_try_wait(fb, issued_parity[s]) && clock64() - t0 < kWaitLimitCycles) {
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t kIdesc = umma_idesc_f16(BM, BN, kBf16);
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+                if (!wait_bar(smem_u32(&bars->tempty[acc]), acc_phase ^ 1u, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+                for (int kt = 0; kt < kt_total; ++kt) {
+                    if (!wait_bar(smem_u32(&bars->full[stage]), phase, abort_flag) ||
+                        !wait_bar(smem_u32(&bars->bfull[stage]), phase, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t adesc = sw128_kmajor_desc(stage_a(stage));
+                    const uint64_t bdesc = sw128_kmajor_desc(stage_b(stage));
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        // advance 16 elements (32 bytes) along K inside the swizzle atom
+                        umma_f16(d_tmem, adesc + 2u * kk, bdesc + 2u * kk, kIdesc, (kt | kk) != 0);
+                    }
+                    umma_commit(smem_u32(&bars->empty[stage]));
+                    if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                umma_commit(smem_u32(&bars->tfull[acc]));
+                if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+            }
+            // every MMA issued by this thread retires before tensor memory is freed
+            umma_commit(smem_u32(&bars->drain));
+            const unsigned long long t0 = clock64();
+            while (!mbar_try_wait(smem_u32(&bars->drain), 0) && clock64() - t0 < kWaitLimitCycles) {
+            }
+        }
+    } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 4) {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;                 // tensor-memory lane quarter of this warp
+        const int row = q * 32 + lane;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
+            const int m_blk = t % num_m, n_blk = t / num_m;
+            if (!wait_bar(smem_u32(&bars->tfull[acc]), acc_phase, abort_flag)) break;
+            tc_fence_after();
+            const int m = m_blk * BM + row;
+            uint16_t* yrow = y + static_cast<size_t>(m) * N;
+#pragma unroll 1
+            for (int ch = 0; ch < BN / 32; ++ch) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                       static_cast<uint32_t>(acc * BN + ch * 32),
+                                   r);
+                tmem_wait_ld();
+                const int n = n_blk * BN + ch * 32;
+                if (m < M) {
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        if (n + 8 * v < N) {
+                            uint4 o;
+                            o.x = Deq<kBf16>::pack2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
+                            o.y = Deq<kBf16>::pack2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
+                            o.z = Deq<kBf16>::pack2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
+                            o.w = Deq<kBf16>::pack2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
+                            *reinterpret_cast<uint4*>(yrow + n + 8 * v) = o;
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(smem_u32(&bars->tempty[acc]));
+            if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        }
+    } else if (warp >= kDeqWarp0) {
+        // ------------------------------------------------------------ dequantisers
+        const int d = threadIdx.x - kDeqWarp0 * 32;    // column of the tile, 0..255
+        const int groups = K / g;
+        int stage = 0;
+        uint32_t phase = 0;
+        for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
+            const int n_blk = t / num_m;
+            const int n = n_blk * BN + d;
+            const bool n_ok = n < N;
+            bool ok = true;
+            // scales / zero-point words of the first K step, then one step ahead
+            auto fetch = [&](int kt, uint32_t& s01, uint32_t& z01) {
+                const int g0 = (kt * BK) / g, g1 = (kt * BK + BK / 2) / g;
+                uint32_t s0 = 0, s1 = 0, z0 = 0, z1 = 0;
+                if (n_ok && g0 < groups) {
+                    s0 = __ldg(sc + static_cast<size_t>(g0) * N + n);
+                    if constexpr (!kSym) z0 = (__ldg(qz + static_cast<size_t>(g0) * (N >> 3) + (n >> 3)) >> (4 * (n & 7))) & 0xFu;
+                }
+                if (n_ok && g1 < groups) {
+                    s1 = __ldg(sc + static_cast<size_t>(g1) * N + n);
+                    if constexpr (!kSym) z1 = (__ldg(qz + static_cast<size_t>(g1) * (N >> 3) + (n >> 3)) >> (4 * (n & 7))) & 0xFu;
+                }
+                if constexpr (kSym) { z0 = 8u; z1 = 8u; }
+                s01 = s0 | (s1 << 16);
+                z01 = z0 | (z1 << 16);
+            };
+            uint32_t s_cur, z_cur, s_nxt = 0, z_nxt = 0;
+            fetch(0, s_cur, z_cur);
+            for (int kt = 0; kt < kt_total; ++kt) {
+                if (kt + 1 < kt_total) fetch(kt + 1, s_nxt, z_nxt);
+                if (!wait_bar(smem_u32(&bars->full[stage]), phase, abort_flag)) { ok = false; break; }
+                const uint32_t* wt = reinterpret_cast<const uint32_t*>(stage_w(stage));
+                const uint32_t b_row = stage_b(stage) + static_cast<uint32_t>(d) * 128u;
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    // words c = 4*half .. 4*half+3 cover K rows [32*half, 32*half + 32) of the step
+                    const uint32_t s16 = half ? (s_cur >> 16) : (s_cur & 0xFFFFu);
+                    const uint32_t z4 = half ? (z_cur >> 16) : (z_cur & 0xFFFFu);
+                    const uint32_t ss = s16 | (s16 << 16);
+                    const uint32_t zz = Deq<kBf16>::kMagic | z4 | (z4 << 16);
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) {
+                        const int c = half * 4 + cc;
+                        const uint32_t w = wt[c * BN + d];
+                        const uint32_t w4 = w >> 4;
+                        uint32_t o[4];
+#pragma unroll
+                        for (int b = 0; b < 4; ++b) {
+                            // byte b of w -> low half, byte b of (w >> 4) -> high half:
+                            // halves (magic + q[8c + 2b], magic + q[8c + 2b + 1])
+                            const uint32_t h = and_or(prmt(w, w4, static_cast<uint32_t>(b | ((4 + b) << 8))),
+                                                      0x000F000Fu, Deq<kBf16>::kMagic);
+                            o[b] = Deq<kBf16>::mul2(Deq<kBf16>::sub2(h, zz), ss);
+                        }
+                        const uint32_t dst = b_row + (static_cast<uint32_t>(c ^ (d & 7)) << 4);
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(o[0]), "r"(o[1]),
+                                     "r"(o[2]), "r"(o[3])
+                                     : "memory");
+                    }
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(smem_u32(&bars->bfull[stage]));
+                if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                s_cur = s_nxt;
+                z_cur = z_nxt;
+            }
+            if (!ok) break;
+        }
+    }
+
+    __syncwarp();   // single-lane roles (producer, MMA issuer) rejoin their warp
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, void* base, uint64_t inner, uint64_t outer,
+               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz) {
+    auto fn = get_encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, dt, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool kBf16, bool kSym>
+cudaError_t launch_typed(const void* x, const uint32_t* qw, const void* sc, const uint32_t* qz, void* y, int M,
+                         int N, int K, int g, const DeviceProps& dp, cudaStream_t s) {
+    auto kern = gemm_kernel<kBf16, kSym>;
+    static int configured_device[64] = {0};
+    if (dp.device >= 0 && dp.device < 64 && !configured_device[dp.device]) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(kSmemBytes));
+        if (e != cudaSuccess) return e;
+        configured_device[dp.device] = 1;
+    }
+    CUtensorMap tx, tw;
+    const CUtensorMapDataType adt = kBf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    if (!encode_2d(&tx, adt, const_cast<void*>(x), (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, BK, BM,
+                   CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    if (!encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_INT32, const_cast<uint32_t*>(qw), (uint64_t)N, (uint64_t)(K / 8),
+                   (uint64_t)N * 4, BN, BK / 8, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+    const int grid = std::max(1, std::min(tiles, dp.sms));
+    kern<<<grid, kThreads, kSmemBytes, s>>>(tx, tw, static_cast<const uint16_t*>(sc), qz, static_cast<uint16_t*>(y),
+                                            M, N, K, g);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const void* x, const uint32_t* qw, const void* sc, const uint32_t* qz, void* y, int M, int N,
+                        int K, int g, bool bf16, const DeviceProps& dp, cudaStream_t s) {
+    if (bf16)
+        return qz ? launch_typed<true, false>(x, qw, sc, qz, y, M, N, K, g, dp, s)
+                  : launch_typed<true, true>(x, qw, sc, qz, y, M, N, K, g, dp, s);
+    return qz ? launch_typed<false, false>(x, qw, sc, qz, y, M, N, K, g, dp, s)
+              : launch_typed<false, true>(x, qw, sc, qz, y, M, N, K, g, dp, s);
+}
+
+cudaError_t read_and_clear_device_error(uint32_t* out, cudaStream_t s) {
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return e;
+    uint32_t v = 0;
+    e = cudaMemcpyFromSymbol(&v, g_device_error, sizeof(v));
+    if (e != cudaSuccess) return e;
+    if (v) {
+        const uint32_t zero = 0;
+        e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof(zero));
+    }
+    *out = v;
+    return e;
+}
+
+}  // namespace w4a16

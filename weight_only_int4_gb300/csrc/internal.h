@@ -1,0 +1,45 @@
+// Launchers shared between the C-ABI layer (api.cu) and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace w4a16 {
+
+struct DeviceProps {
+    int device = -1;
+    int sms = 0;
+    int cc_major = 0;
+    int cc_minor = 0;
+    size_t smem_optin = 0;
+};
+
+// Properties of the current device, cached per device ordinal.
+cudaError_t current_device_props(DeviceProps* out);
+
+cudaError_t launch_pack(const uint8_t* src, uint32_t* dst, int64_t rows, int64_t cols, int dim,
+                        const DeviceProps& dp, cudaStream_t s);
+cudaError_t launch_unpack(const uint32_t* src, uint8_t* dst, int64_t rows, int64_t cols, int dim,
+                          const DeviceProps& dp, cudaStream_t s);
+
+struct GemvPlan {
+    int mt = 0;        // row template (>= M)
+    int cols = 0;      // columns per lane
+    int cb = 0;        // columns per column block (32 * cols)
+    int n_cb = 0;      // column blocks
+    int cluster = 1;   // CTAs per cluster along K
+    int warps = 8;     // warps per CTA
+};
+
+GemvPlan plan_gemv(int M, int N, int K, int g, const DeviceProps& dp);
+
+cudaError_t launch_gemv(const void* x, const uint32_t* qw, const void* sc, const uint32_t* qz, void* y,
+                        int M, int N, int K, int g, bool bf16, const GemvPlan& plan, cudaStream_t s);
+
+cudaError_t launch_gemm(const void* x, const uint32_t* qw, const void* sc, const uint32_t* qz, void* y,
+                        int M, int N, int K, int g, bool bf16, const DeviceProps& dp, cudaStream_t s);
+
+// Read and clear the device-side error word of the GEMM pipeline (after a sync).
+cudaError_t read_and_clear_device_error(uint32_t* out, cudaStream_t s);
+
+}  // namespace w4a16
