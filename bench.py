@@ -152,13 +152,16 @@ class Layer:
                                         for _ in range(copies - 1)]
         self.y = [torch.empty((wl.M, wl.N), dtype=self.x.dtype, device="cuda") for _ in range(copies)]
         self.fn = getattr(w4, wl.kernel)
+        op = w4.OP_GEMV if wl.kernel == "gemv" else w4.OP_GEMM
+        nws = w4.workspace_bytes(op, wl.M, wl.N, wl.K, wl.g)
+        self.ws = w4.new_workspace(nws) if nws else None
         self.bytes = layer_bytes(wl.M, wl.N, wl.K, wl.g, wl.symmetric, wl.act)
         self.flops = layer_flops(wl.M, wl.N, wl.K)
 
     def step(self, x=None):
         x = self.x if x is None else x
         for (qw, s, qz), y in zip(self.weights, self.y):
-            self.fn(x, qw, s, qz, self.wl.g, out=y)
+            self.fn(x, qw, s, qz, self.wl.g, out=y, workspace=self.ws)
 
 
 def time_graph(layer, steps, warmup, torch, barrier):

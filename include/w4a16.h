@@ -31,8 +31,8 @@
  *
  * Conventions for every entry point below:
  *   - Every tensor pointer is a DEVICE pointer owned by the caller; tensors
- *     are dense and row-major. The library never allocates, frees or
- *     synchronises device memory, except w4a16_device_status, which
+ *     are dense and row-major. The library never allocates or frees device
+ *     memory and never synchronises, except w4a16_device_status, which
  *     synchronises the given stream.
  *   - Calls are asynchronous on `stream` (NULL = the legacy default stream).
  *   - All argument checks run on the host BEFORE anything is launched; a
@@ -111,30 +111,43 @@ w4a16_status w4a16_unpack(const int32_t* src, uint8_t* dst, int64_t rows, int64_
                           w4a16_stream stream);
 
 /*
- * w4a16_workspace_bytes -- device workspace the op needs for this shape on
- * the current device (0 if none). The GEMV and the GEMM of this build need
- * none; the argument exists so a caller can size a workspace without knowing
- * which kernel variant runs. Returns 0 for invalid shapes.
+ * w4a16_workspace_bytes -- bytes of device workspace `op` needs for this shape
+ * on the current device; 0 for the GEMM. For the GEMV: a region of FP32
+ * partial-sum slots whose size depends only on the device (16 KB per SM),
+ * followed by one 32-bit ticket per column block of the shape (rounded up to
+ * 256 bytes). Returns 0 for shapes the op rejects and when no GB300 is
+ * current.
  */
 size_t w4a16_workspace_bytes(w4a16_op op, int64_t M, int64_t N, int64_t K, int64_t g);
 
 /*
  * w4a16_gemv -- decode path, 1 <= M <= 16.
  *
- * Streams qweight, scales and qzeros once with 128-bit coalesced loads, splits
- * K across the warps of a thread-block cluster and reduces the partial sums
- * through shared and distributed shared memory in a fixed order (the result
- * is deterministic). This is the memory-bound skinny kernel that the
- * zero-point page measures ("Results" and "Known regression").
+ * Streams qweight, scales and qzeros once with 128-bit coalesced loads; the
+ * loads of the next 32-row chunk of K are in flight while the current one is
+ * converted, which is the overlap whose absence the zero-point page blames for
+ * its batch-4, g=128 regression (section "Known regression"). A persistent
+ * grid of two CTAs per SM takes equal shares of (column block, K chunk) items,
+ * so every SM streams the same bytes; a column block shared by several CTAs
+ * is finished by the last of them to arrive, which sums the partial vectors
+ * in ascending CTA order: the result is deterministic.
  *
  * x        [M, K] dtype `dt`
  * qweight  int32 [K/8, N]
  * scales   [K/g, N] dtype `dt`
  * qzeros   int32 [K/g, N/8], or NULL for the symmetric layer (z = 8)
  * y        [M, N] dtype `dt`, written (not accumulated into)
- * workspace, workspace_bytes   unused by this build; may be NULL / 0
+ * workspace, workspace_bytes   device scratch of at least
+ *          w4a16_workspace_bytes(W4A16_OP_GEMV, M, N, K, g) bytes, 16-byte
+ *          aligned, owned by the caller. It must be zero-filled before its
+ *          first use; every call leaves its ticket words at zero again and
+ *          writes partial sums only below the ticket region, so one
+ *          workspace sized for the largest N serves any later call of any
+ *          shape. Two calls that may run at the same time (different
+ *          streams) must not share a workspace.
  * Errors: NULL, SHAPE (M outside 1..16, N % 8, K % g), UNSUPPORTED (g not in
- * {32, 64, 128, 256}), DTYPE, ALIGN, WORKSPACE, DEVICE, CUDA.
+ * {32, 64, 128, 256}), DTYPE, ALIGN, WORKSPACE (NULL, unaligned or too small),
+ * DEVICE, CUDA.
  */
 w4a16_status w4a16_gemv(const void* x, const int32_t* qweight, const void* scales,
                         const int32_t* qzeros, void* y, int64_t M, int64_t N, int64_t K,

@@ -50,13 +50,13 @@ class DeviceCase:
         return O.reference_rows(self.case.x, rows, qw, self.case.s, qz, self.g, self.act)
 
 
-def guarded_out(M: int, N: int, dtype, pad: int = 1024, sentinel: float = 12345.0):
+def guarded_out(M: int, N: int, dtype, pad: int = 1024, sentinel: float = -1536.0):
     """Output [M, N] inside a sentinel-filled buffer (16-byte aligned view)."""
     buf = torch.full((M * N + 2 * pad,), sentinel, dtype=dtype, device="cuda")
     return buf, buf[pad:pad + M * N].view(M, N), pad
 
 
-def check_guards(buf: torch.Tensor, pad: int, sentinel: float = 12345.0):
+def check_guards(buf: torch.Tensor, pad: int, sentinel: float = -1536.0):
     head = buf[:pad].float().cpu()
     tail = buf[-pad:].float().cpu()
     assert torch.all(head == sentinel), "write before the output buffer"

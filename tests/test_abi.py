@@ -51,7 +51,7 @@ def _gemv(lib, **kw):
     a = dict(x=P, qw=P, s=P, z=P, y=P, M=1, N=64, K=128, g=32, dt=w4.F16)
     a.update(kw)
     return lib.w4a16_gemv(a["x"], a["qw"], a["s"], a["z"], a["y"], a["M"], a["N"], a["K"], a["g"],
-                          a["dt"], None, 0, None)
+                          a["dt"], a.get("ws", P), a.get("ws_bytes", 1 << 30), None)
 
 
 def _gemm(lib, **kw):
@@ -82,6 +82,11 @@ def test_layer_rejections(lib, call):
 
 def test_gemv_row_limit(lib):
     assert _gemv(lib, M=17) == w4.ERR_SHAPE
+
+
+def test_gemv_needs_an_aligned_workspace(lib):
+    assert _gemv(lib, ws=None) == w4.ERR_WORKSPACE
+    assert _gemv(lib, ws=MIS) == w4.ERR_WORKSPACE
 
 
 def test_pack_rejections(lib):

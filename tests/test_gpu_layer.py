@@ -114,14 +114,35 @@ def test_onehot_bit_exact(op, act, sym):
         assert np.array_equal(y[m], want), (op, act, sym, m)
 
 
-@pytest.mark.parametrize("op", ["gemv", "gemm"])
+@pytest.mark.parametrize("op,M", [("gemv", 6), ("gemv", 16), ("gemm", 200)])
 @pytest.mark.parametrize("act", ["f16", "bf16"])
-def test_q_equals_z_is_exactly_zero(op, act):
-    M = 3 if op == "gemv" else 200
+def test_q_equals_z_is_exactly_zero(op, M, act):
+    """Paths that subtract z from each nibble in 16-bit arithmetic give exact zeros."""
     case = make_case(M, 264, 256, 32, act, False, seed=23)
     case.q = np.repeat(case.z, 32, axis=0)
     y = run(op, DeviceCase(case))
     assert torch.count_nonzero(y).item() == 0
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 4])
+@pytest.mark.parametrize("act", ["f16", "bf16"])
+def test_q_equals_z_gemv_chunk_sums(M, act):
+    """For M <= 4 the GEMV applies z once per 32-row chunk as (magic + z) * sum(x):
+    q == z then gives zero up to FP32 rounding of two sums of size magic * sum|x|.
+    Bound: 64 FP32 half-ulps of magic * sum|x| per chunk (32 additions into two sums
+    and their difference), times max|s|, summed over the chunks."""
+    K = 1024
+    case = make_case(M, 264, K, 32, act, False, seed=29)
+    ref_scale = np.abs(DeviceCase(case).reference()).max()
+    case.q = np.repeat(case.z, 32, axis=0)
+    y = torch_to_f64(run("gemv", DeviceCase(case)))
+    x = O.widen(case.x, act)
+    magic = 1024.0 if act == "f16" else 128.0
+    s_max = np.abs(O.widen(case.s, act)).max()
+    chunk_abs = np.abs(x).reshape(M, K // 32, 32).sum(axis=2)          # [M, chunks]
+    bound = 64 * 2.0 ** -23 * magic * s_max * chunk_abs.sum(axis=1).max()
+    assert np.abs(y).max() <= bound, (np.abs(y).max(), bound)
+    assert np.abs(y).max() <= 1e-3 * ref_scale
 
 
 @pytest.mark.parametrize("op,M", [("gemv", 4), ("gemm", 300)])
@@ -138,6 +159,28 @@ def test_gemv_and_gemm_agree():
     b = torch_to_f64(w4.gemm(dc.x, dc.qw, dc.s, dc.qz, 32))
     ref = dc.reference()
     assert np.abs(a - b).max() <= 2 * 1.6e-2 * np.abs(ref).max()
+
+
+def test_gemv_workspace_reuse_across_shapes():
+    """One workspace serves calls of different shapes: every call leaves its tickets at zero."""
+    ws = w4.new_workspace(8 << 20)
+    cases = [DeviceCase(make_case(M, N, K, 32, "f16", False, seed=M + N))
+             for (M, N, K) in ((1, 4104, 2048), (3, 1032, 4096), (1, 43008, 512), (7, 264, 256))]
+    for _ in range(2):
+        for dc in cases:
+            need = w4.workspace_bytes(w4.OP_GEMV, dc.case.M, dc.case.N, dc.case.K, 32)
+            assert 0 < need <= ws.numel()
+            y = w4.gemv(dc.x, dc.qw, dc.s, dc.qz, 32, workspace=ws)
+            assert_within_tol(y, dc.reference(), "f16", "reuse")
+
+
+def test_gemv_workspace_too_small():
+    dc = DeviceCase(make_case(1, 2048, 2048, 128, "f16", False, seed=0))
+    need = w4.workspace_bytes(w4.OP_GEMV, 1, 2048, 2048, 128)
+    small = w4.new_workspace(max(16, need - 256))
+    with pytest.raises(w4.W4A16Error) as e:
+        w4.gemv(dc.x, dc.qw, dc.s, dc.qz, 128, workspace=small)
+    assert e.value.status == w4.ERR_WORKSPACE
 
 
 def test_binding_rejections():

@@ -155,7 +155,30 @@ def unpack(words, dim: int, out=None, stream=None):
 
 
 def workspace_bytes(op: int, M: int, N: int, K: int, g: int) -> int:
+    """Device workspace the op needs on the current device (0 if none)."""
     return int(load_library().w4a16_workspace_bytes(op, M, N, K, g))
+
+
+def new_workspace(nbytes: int, device=None):
+    """A zero-filled uint8 device workspace. Calls leave it zeroed where it must
+    start at zero, so one workspace serves any number of calls, as long as no
+    two calls that use it run at the same time."""
+    torch = _torch()
+    return torch.zeros(max(int(nbytes), 16), dtype=torch.uint8,
+                       device=torch.device("cuda") if device is None else device)
+
+
+_workspaces = {}
+
+
+def _cached_workspace(nbytes: int, device, stream_ptr: int):
+    """One growing workspace per (device, stream): calls on one stream never overlap."""
+    key = (device.index if device.index is not None else _torch().cuda.current_device(), stream_ptr)
+    ws = _workspaces.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = new_workspace(nbytes, device)
+        _workspaces[key] = ws
+    return ws
 
 
 def _layer(fn_name: str, x, qweight, scales, qzeros, group_size: int, out=None, workspace=None,
@@ -188,11 +211,15 @@ def _layer(fn_name: str, x, qweight, scales, qzeros, group_size: int, out=None, 
     if out is None:
         out = torch.empty((M, N), dtype=x.dtype, device=x.device)
     _cuda_contig("out", out)
+    lib = load_library()
+    sp = _stream_ptr(stream)
+    if workspace is None:
+        need = lib.w4a16_workspace_bytes(OP_GEMV if fn_name == "w4a16_gemv" else OP_GEMM, M, N, K, group_size)
+        workspace = _cached_workspace(need, x.device, sp) if need else None
     ws_ptr, ws_bytes = (0, 0) if workspace is None else (workspace.data_ptr(),
                                                           workspace.numel() * workspace.element_size())
-    fn = getattr(load_library(), fn_name)
-    _check(fn_name, fn(x.data_ptr(), qweight.data_ptr(), scales.data_ptr(), zp, out.data_ptr(),
-                       M, N, K, group_size, dt, ws_ptr, ws_bytes, _stream_ptr(stream)))
+    _check(fn_name, getattr(lib, fn_name)(x.data_ptr(), qweight.data_ptr(), scales.data_ptr(), zp,
+                                          out.data_ptr(), M, N, K, group_size, dt, ws_ptr, ws_bytes, sp))
     return out
 
 

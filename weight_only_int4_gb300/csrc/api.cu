@@ -123,27 +123,27 @@ w4a16_status w4a16_unpack(const int32_t* src, uint8_t* dst, int64_t rows, int64_
 }
 
 size_t w4a16_workspace_bytes(w4a16_op op, int64_t M, int64_t N, int64_t K, int64_t g) {
-    (void)op;
-    (void)M;
-    (void)N;
-    (void)K;
-    (void)g;
-    return 0;
+    if (op != W4A16_OP_GEMV) return 0;
+    if (M < 1 || M > 16 || N < 8 || N % 8 || K < 1 || K > kMaxDim || N > kMaxDim || !supported_group(g) || K % g)
+        return 0;
+    DeviceProps dp;
+    if (device_gate(&dp) != W4A16_OK) return 0;
+    return w4a16::gemv_workspace_bytes(w4a16::plan_gemv((int)M, (int)N, (int)K, (int)g, dp));
 }
 
 w4a16_status w4a16_gemv(const void* x, const int32_t* qweight, const void* scales, const int32_t* qzeros, void* y,
                         int64_t M, int64_t N, int64_t K, int64_t g, w4a16_dtype dt, void* workspace,
                         size_t workspace_bytes, w4a16_stream stream) {
-    (void)workspace;
-    (void)workspace_bytes;
     w4a16_status st = check_layer_args(x, qweight, scales, qzeros, y, M, N, K, g, dt, 16);
     if (st != W4A16_OK) return st;
+    if (!workspace || !aligned16(workspace)) return W4A16_ERR_WORKSPACE;
     DeviceProps dp;
     if ((st = device_gate(&dp)) != W4A16_OK) return st;
     const w4a16::GemvPlan plan = w4a16::plan_gemv((int)M, (int)N, (int)K, (int)g, dp);
+    if (workspace_bytes < w4a16::gemv_workspace_bytes(plan)) return W4A16_ERR_WORKSPACE;
     return from_cuda(w4a16::launch_gemv(x, reinterpret_cast<const uint32_t*>(qweight), scales,
                                         reinterpret_cast<const uint32_t*>(qzeros), y, (int)M, (int)N, (int)K, (int)g,
-                                        dt == W4A16_BF16, plan, reinterpret_cast<cudaStream_t>(stream)));
+                                        dt == W4A16_BF16, plan, workspace, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 w4a16_status w4a16_gemm(const void* x, const int32_t* qweight, const void* scales, const int32_t* qzeros, void* y,

@@ -44,31 +44,37 @@ __device__ unsigned int g_device_error = 0;
 namespace {
 
 constexpr int BM = 128, BN = 256, BK = 64;
-constexpr int kStages = 3;
+constexpr int kLoadStages = 4;           // x tile + packed weights + scales + zero-points
+constexpr int kBStages = 3;              // dequantised operand tiles
 constexpr int kThreads = 512;
 constexpr int kEpiWarp0 = 4;             // warps 4..7
 constexpr int kDeqWarp0 = 8;             // warps 8..15
-constexpr int kDeqThreads = 256;         // one dequant thread per column of the tile
+constexpr int kDeqWarps = 8;             // one dequant thread per column of the tile
 constexpr uint32_t kABytes = BM * BK * 2;            // 16 KB
-constexpr uint32_t kBBytes = BN * BK * 2;            // 32 KB
 constexpr uint32_t kWBytes = (BK / 8) * BN * 4;      //  8 KB
-constexpr uint32_t kStageBytes = kABytes + kBBytes + kWBytes;
+constexpr uint32_t kSBytes = 2 * BN * 2;             //  1 KB: scales of the two 32-row halves of a step
+constexpr uint32_t kZBytes = 2 * (BN / 8) * 4;       // 256 B: zero-point words of the two halves
+constexpr uint32_t kLoadStageBytes = (kABytes + kWBytes + kSBytes + kZBytes + 1023) & ~1023u;
+constexpr uint32_t kBBytes = BN * BK * 2;            // 32 KB
 constexpr uint32_t kTmemCols = 2 * BN;               // two accumulators
 constexpr unsigned long long kWaitLimitCycles = 4000000000ull;   // ~2 s at 2 GHz
 constexpr unsigned int kErrTimeout = 9u;
 
 struct __align__(8) Barriers {
-    uint64_t full[kStages];     // TMA bytes landed (x tile + packed weight tile)
-    uint64_t bfull[kStages];    // dequantised operand tile written (256 arrivals)
-    uint64_t empty[kStages];    // MMAs reading the stage retired (tcgen05.commit)
-    uint64_t tfull[2];          // accumulator complete
-    uint64_t tempty[2];         // accumulator drained by the epilogue (128 arrivals)
-    uint64_t drain;             // final commit of the MMA thread
+    uint64_t lfull[kLoadStages];    // x + weights (TMA bytes) and scales/zero-points (cp.async) landed
+    uint64_t lempty[kLoadStages];   // MMAs reading the x tile retired (tcgen05.commit)
+    uint64_t bfull[kBStages];       // dequantised operand tile written (one arrival per dequant warp)
+    uint64_t bempty[kBStages];      // MMAs reading the operand tile retired (tcgen05.commit)
+    uint64_t tfull[2];              // accumulator complete
+    uint64_t tempty[2];             // accumulator drained by the epilogue (one arrival per epilogue warp)
+    uint64_t drain;                 // final commit of the MMA thread
     uint32_t tmem_base;
     int abort;
 };
 
-constexpr size_t kSmemBytes = 1024 /*align slack*/ + kStages * kStageBytes + sizeof(Barriers);
+constexpr size_t kSmemBytes =
+    1024 /*align slack*/ + kLoadStages * kLoadStageBytes + kBStages * kBBytes + sizeof(Barriers);
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
 // Bounded wait: false if the wait ran out (or another role already gave up).
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort) {
@@ -85,6 +91,20 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
             }
         }
     }
+}
+
+// Lane 0 waits (bounded); then every lane of the warp observes the completed
+// phase itself. Returns the same verdict in every lane.
+__device__ __forceinline__ bool warp_wait_bar(uint32_t bar, uint32_t parity, volatile int* abort, int lane) {
+    int ok = 1;
+    if (lane == 0) ok = wait_bar(bar, parity, abort) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (ok && lane != 0) {
+        // the phase is already complete: this succeeds at once; bounded all the same
+        for (uint32_t i = 0; !mbar_try_wait(bar, parity) && i < (1u << 20); ++i) {
+        }
+    }
+    return ok != 0;
 }
 
 template <bool kBf16>
@@ -133,27 +153,36 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
             int N, int K, int g) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    Barriers* bars = reinterpret_cast<Barriers*>(smem + kStages * kStageBytes);
+    uint8_t* bsmem = smem + kLoadStages * kLoadStageBytes;
+    Barriers* bars = reinterpret_cast<Barriers*>(bsmem + kBStages * kBBytes);
     const uint32_t smem_base = smem_u32(smem);
-    auto stage_a = [&](int s) { return smem_base + s * kStageBytes; };
-    auto stage_b = [&](int s) { return smem_base + s * kStageBytes + kABytes; };
-    auto stage_w = [&](int s) { return smem + s * kStageBytes + kABytes + kBBytes; };
+    const uint32_t bsmem_base = smem_u32(bsmem);
+    // load stage s: [x tile | packed weights | scales | zero-point words]
+    auto ld_a = [&](int s) { return smem_base + s * kLoadStageBytes; };
+    auto ld_w = [&](int s) { return smem + s * kLoadStageBytes + kABytes; };
+    auto ld_s = [&](int s) { return smem + s * kLoadStageBytes + kABytes + kWBytes; };
+    auto ld_z = [&](int s) { return smem + s * kLoadStageBytes + kABytes + kWBytes + kSBytes; };
+    auto op_b = [&](int s) { return bsmem_base + s * kBBytes; };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int num_m = (M + BM - 1) / BM, num_n = (N + BN - 1) / BN;
     const int tiles = num_m * num_n;
     const int kt_total = (K + BK - 1) / BK;
+    const int groups = K / g;
     volatile int* abort_flag = &bars->abort;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(smem_u32(&bars->full[s]), 1);
-            mbar_init(smem_u32(&bars->bfull[s]), kDeqThreads);
-            mbar_init(smem_u32(&bars->empty[s]), 1);
+        for (int s = 0; s < kLoadStages; ++s) {
+            mbar_init(smem_u32(&bars->lfull[s]), 1);
+            mbar_init(smem_u32(&bars->lempty[s]), 1);
+        }
+        for (int s = 0; s < kBStages; ++s) {
+            mbar_init(smem_u32(&bars->bfull[s]), kDeqWarps);
+            mbar_init(smem_u32(&bars->bempty[s]), 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(smem_u32(&bars->tfull[a]), 1);
-            mbar_init(smem_u32(&bars->tempty[a]), 128);
+            mbar_init(smem_u32(&bars->tempty[a]), 4);
         }
         mbar_init(smem_u32(&bars->drain), 1);
         bars->abort = 0;
@@ -168,31 +197,50 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
     const uint32_t tmem_base = bars->tmem_base;
 
     if (warp == 0) {
-        // ------------------------------------------------------------ TMA producer
-        if (lane == 0) {
-            int stage = 0;
-            uint32_t phase = 0;
-            uint32_t issued_parity[kStages];
-            bool issued[kStages];
-            for (int s = 0; s < kStages; ++s) issued[s] = false, issued_parity[s] = 0;
-            bool ok = true;
-            for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
-                const int m_blk = t % num_m, n_blk = t / num_m;
-                for (int kt = 0; kt < kt_total; ++kt) {
-                    if (!wait_bar(smem_u32(&bars->empty[stage]), phase ^ 1u, abort_flag)) { ok = false; break; }
-                    const uint32_t fb = smem_u32(&bars->full[stage]);
-                    mbar_arrive_expect_tx(fb, kABytes + kWBytes);
-                    tma_load_2d(stage_a(stage), &tmap_x, kt * BK, m_blk * BM, fb);
-                    tma_load_2d(smem_u32(stage_w(stage)), &tmap_w, n_blk * BN, kt * (BK / 8), fb);
-                    issued[stage] = true;
-                    issued_parity[stage] = phase;
-                    if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        // ------------------------------------------------------------ producer warp
+        // lane l stages the scales of columns [8l, 8l+8) and their zero-point word
+        // with cp.async (zero-filled outside N and K); lane 0 then issues the TMA
+        // copies of the x tile and the packed weight tile.
+        int stage = 0;
+        uint32_t phase = 0;
+        uint32_t issued_parity[kLoadStages];
+        bool issued[kLoadStages];
+        for (int s = 0; s < kLoadStages; ++s) issued[s] = false, issued_parity[s] = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+            const int m_blk = t % num_m, n_blk = t / num_m;
+            const int n = n_blk * BN + 8 * lane;
+            for (int kt = 0; kt < kt_total; ++kt) {
+                if (!warp_wait_bar(smem_u32(&bars->lempty[stage]), phase ^ 1u, abort_flag, lane)) { ok = false; break; }
+                const uint32_t fb = smem_u32(&bars->lfull[stage]);
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    const int grp = (kt * BK + half * (BK / 2)) / g;
+                    const bool valid = n < N && grp < groups;
+                    const size_t so = valid ? static_cast<size_t>(grp) * N + n : 0;
+                    cp_async_16(smem_u32(ld_s(stage)) + half * (BN * 2) + 16 * lane, sc + so, valid ? 16u : 0u);
+                    if constexpr (!kSym) {
+                        const size_t zo = valid ? static_cast<size_t>(grp) * (N >> 3) + (n >> 3) : 0;
+                        cp_async_4(smem_u32(ld_z(stage)) + half * (BN / 8) * 4 + 4 * lane, qz + zo, valid ? 4u : 0u);
+                    }
                 }
+                cp_async_mbar_arrive(fb);
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(fb, kABytes + kWBytes);
+                    tma_load_2d(ld_a(stage), &tmap_x, kt * BK, m_blk * BM, fb);
+                    tma_load_2d(smem_u32(ld_w(stage)), &tmap_w, n_blk * BN, kt * (BK / 8), fb);
+                }
+                issued[stage] = true;
+                issued_parity[stage] = phase;
+                if (++stage == kLoadStages) { stage = 0; phase ^= 1u; }
             }
-            // copies still in flight must land before this CTA's shared memory is released
-            for (int s = 0; s < kStages; ++s) {
+        }
+        // copies still in flight must land before this CTA's shared memory is released
+        if (lane == 0) {
+            for (int s = 0; s < kLoadStages; ++s) {
                 if (!issued[s]) continue;
-                const uint32_t fb = smem_u32(&bars->full[s]);
+                const uint32_t fb = smem_u32(&bars->lfull[s]);
                 const unsigned long long t0 = clock64();
                 while (!mbar_try_wait(fb, issued_parity[s]) && clock64() - t0 < kWaitLimitCycles) {
                 }
@@ -202,8 +250,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t kIdesc = umma_idesc_f16(BM, BN, kBf16);
-            int stage = 0;
-            uint32_t phase = 0;
+            int ls = 0, bs = 0;
+            uint32_t lph = 0, bph = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
@@ -212,21 +260,23 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
                 for (int kt = 0; kt < kt_total; ++kt) {
-                    if (!wait_bar(smem_u32(&bars->full[stage]), phase, abort_flag) ||
-                        !wait_bar(smem_u32(&bars->bfull[stage]), phase, abort_flag)) {
+                    if (!wait_bar(smem_u32(&bars->lfull[ls]), lph, abort_flag) ||
+                        !wait_bar(smem_u32(&bars->bfull[bs]), bph, abort_flag)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t adesc = sw128_kmajor_desc(stage_a(stage));
-                    const uint64_t bdesc = sw128_kmajor_desc(stage_b(stage));
+                    const uint64_t adesc = sw128_kmajor_desc(ld_a(ls));
+                    const uint64_t bdesc = sw128_kmajor_desc(op_b(bs));
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk) {
                         // advance 16 elements (32 bytes) along K inside the swizzle atom
                         umma_f16(d_tmem, adesc + 2u * kk, bdesc + 2u * kk, kIdesc, (kt | kk) != 0);
                     }
-                    umma_commit(smem_u32(&bars->empty[stage]));
-                    if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                    umma_commit(smem_u32(&bars->lempty[ls]));
+                    umma_commit(smem_u32(&bars->bempty[bs]));
+                    if (++ls == kLoadStages) { ls = 0; lph ^= 1u; }
+                    if (++bs == kBStages) { bs = 0; bph ^= 1u; }
                 }
                 if (!ok) break;
                 umma_commit(smem_u32(&bars->tfull[acc]));
@@ -246,7 +296,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
         uint32_t acc_phase = 0;
         for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
             const int m_blk = t % num_m, n_blk = t / num_m;
-            if (!wait_bar(smem_u32(&bars->tfull[acc]), acc_phase, abort_flag)) break;
+            if (!warp_wait_bar(smem_u32(&bars->tfull[acc]), acc_phase, abort_flag, lane)) break;
             tc_fence_after();
             const int m = m_blk * BM + row;
             uint16_t* yrow = y + static_cast<size_t>(m) * N;
@@ -273,48 +323,32 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
                 }
             }
             tc_fence_before();
-            mbar_arrive(smem_u32(&bars->tempty[acc]));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&bars->tempty[acc]));
             if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
         }
     } else if (warp >= kDeqWarp0) {
         // ------------------------------------------------------------ dequantisers
         const int d = threadIdx.x - kDeqWarp0 * 32;    // column of the tile, 0..255
-        const int groups = K / g;
-        int stage = 0;
-        uint32_t phase = 0;
-        for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
-            const int n_blk = t / num_m;
-            const int n = n_blk * BN + d;
-            const bool n_ok = n < N;
-            bool ok = true;
-            // scales / zero-point words of the first K step, then one step ahead
-            auto fetch = [&](int kt, uint32_t& s01, uint32_t& z01) {
-                const int g0 = (kt * BK) / g, g1 = (kt * BK + BK / 2) / g;
-                uint32_t s0 = 0, s1 = 0, z0 = 0, z1 = 0;
-                if (n_ok && g0 < groups) {
-                    s0 = __ldg(sc + static_cast<size_t>(g0) * N + n);
-                    if constexpr (!kSym) z0 = (__ldg(qz + static_cast<size_t>(g0) * (N >> 3) + (n >> 3)) >> (4 * (n & 7))) & 0xFu;
-                }
-                if (n_ok && g1 < groups) {
-                    s1 = __ldg(sc + static_cast<size_t>(g1) * N + n);
-                    if constexpr (!kSym) z1 = (__ldg(qz + static_cast<size_t>(g1) * (N >> 3) + (n >> 3)) >> (4 * (n & 7))) & 0xFu;
-                }
-                if constexpr (kSym) { z0 = 8u; z1 = 8u; }
-                s01 = s0 | (s1 << 16);
-                z01 = z0 | (z1 << 16);
-            };
-            uint32_t s_cur, z_cur, s_nxt = 0, z_nxt = 0;
-            fetch(0, s_cur, z_cur);
+        int ls = 0, bs = 0;
+        uint32_t lph = 0, bph = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
             for (int kt = 0; kt < kt_total; ++kt) {
-                if (kt + 1 < kt_total) fetch(kt + 1, s_nxt, z_nxt);
-                if (!wait_bar(smem_u32(&bars->full[stage]), phase, abort_flag)) { ok = false; break; }
-                const uint32_t* wt = reinterpret_cast<const uint32_t*>(stage_w(stage));
-                const uint32_t b_row = stage_b(stage) + static_cast<uint32_t>(d) * 128u;
+                if (!warp_wait_bar(smem_u32(&bars->lfull[ls]), lph, abort_flag, lane) ||
+                    !warp_wait_bar(smem_u32(&bars->bempty[bs]), bph ^ 1u, abort_flag, lane)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t* wt = reinterpret_cast<const uint32_t*>(ld_w(ls));
+                const uint16_t* st = reinterpret_cast<const uint16_t*>(ld_s(ls));
+                const uint32_t* zt = reinterpret_cast<const uint32_t*>(ld_z(ls));
+                const uint32_t b_row = op_b(bs) + static_cast<uint32_t>(d) * 128u;
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     // words c = 4*half .. 4*half+3 cover K rows [32*half, 32*half + 32) of the step
-                    const uint32_t s16 = half ? (s_cur >> 16) : (s_cur & 0xFFFFu);
-                    const uint32_t z4 = half ? (z_cur >> 16) : (z_cur & 0xFFFFu);
+                    const uint32_t s16 = st[half * BN + d];
+                    const uint32_t z4 = kSym ? 8u : ((zt[half * (BN / 8) + (d >> 3)] >> (4 * (d & 7))) & 0xFu);
                     const uint32_t ss = s16 | (s16 << 16);
                     const uint32_t zz = Deq<kBf16>::kMagic | z4 | (z4 << 16);
 #pragma unroll
@@ -338,16 +372,15 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
                     }
                 }
                 fence_proxy_async_smem();
-                mbar_arrive(smem_u32(&bars->bfull[stage]));
-                if (++stage == kStages) { stage = 0; phase ^= 1u; }
-                s_cur = s_nxt;
-                z_cur = z_nxt;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&bars->bfull[bs]));
+                if (++ls == kLoadStages) { ls = 0; lph ^= 1u; }
+                if (++bs == kBStages) { bs = 0; bph ^= 1u; }
             }
-            if (!ok) break;
         }
     }
 
-    __syncwarp();   // single-lane roles (producer, MMA issuer) rejoin their warp
+    __syncwarp();   // single-lane roles (MMA issuer) rejoin their warp
     tc_fence_before();
     __syncthreads();
     if (warp == 2) {

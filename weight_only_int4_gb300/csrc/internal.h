@@ -23,18 +23,28 @@ cudaError_t launch_unpack(const uint32_t* src, uint8_t* dst, int64_t rows, int64
                           const DeviceProps& dp, cudaStream_t s);
 
 struct GemvPlan {
-    int mt = 0;        // row template (>= M)
-    int cols = 0;      // columns per lane
-    int cb = 0;        // columns per column block (32 * cols)
-    int n_cb = 0;      // column blocks
-    int cluster = 1;   // CTAs per cluster along K
-    int warps = 8;     // warps per CTA
+    int mt = 0;             // row template (>= M)
+    int cols = 0;           // columns per lane
+    int cb = 0;             // columns per column block (32 * cols)
+    int n_cb = 0;           // column blocks
+    int warps = 8;          // warps per CTA
+    int grid = 0;           // persistent CTAs (two per SM at most)
+    long long items = 0;    // column blocks x 32-row chunks of K
+    bool fact = false;      // zero-point applied per chunk through chunk sums of x
+    size_t smem_bytes = 0;  // dynamic shared memory per CTA
+    size_t ticket_bytes = 0;
+    size_t partial_bytes = 0;
 };
 
 GemvPlan plan_gemv(int M, int N, int K, int g, const DeviceProps& dp);
+size_t gemv_workspace_bytes(const GemvPlan& plan);
 
+// `workspace` holds plan.partial_bytes of partial-sum slots (a size fixed per
+// device) followed by plan.ticket_bytes of ticket words (zero before the first
+// call; every call leaves them zero).
 cudaError_t launch_gemv(const void* x, const uint32_t* qw, const void* sc, const uint32_t* qz, void* y,
-                        int M, int N, int K, int g, bool bf16, const GemvPlan& plan, cudaStream_t s);
+                        int M, int N, int K, int g, bool bf16, const GemvPlan& plan, void* workspace,
+                        cudaStream_t s);
 
 cudaError_t launch_gemm(const void* x, const uint32_t* qw, const void* sc, const uint32_t* qz, void* y,
                         int M, int N, int K, int g, bool bf16, const DeviceProps& dp, cudaStream_t s);

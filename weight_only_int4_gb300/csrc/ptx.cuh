@@ -61,6 +61,23 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int3
 }
 
 // ---------------------------------------------------------------------------
+// cp.async (LDGSTS): small asynchronous copies with zero fill, tracked by an mbarrier
+// ---------------------------------------------------------------------------
+// Copy `src_bytes` (0 or 16) of the 16 bytes at src to dst; the rest is zero-filled.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+// Copy `src_bytes` (0 or 4) of the 4 bytes at src to dst; the rest is zero-filled.
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+// Arrive on `bar` once every cp.async issued so far by this thread has landed. The
+// pending count is raised first, so the barrier's expected arrival count is unchanged.
+__device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// ---------------------------------------------------------------------------
 // fences
 // ---------------------------------------------------------------------------
 // Make this thread's generic-proxy shared-memory writes visible to the async
