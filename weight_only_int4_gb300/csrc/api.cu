@@ -164,10 +164,11 @@ w4a16_status w4a16_device_status(w4a16_stream stream) {
     DeviceProps dp;
     w4a16_status st = device_gate(&dp);
     if (st != W4A16_OK) return st;
-    uint32_t v = 0;
-    if (w4a16::read_and_clear_device_error(&v, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    uint32_t v = 0, u = 0;
+    if (w4a16::read_and_clear_device_error(&v, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess ||
+        w4a16::read_and_clear_gemv_error(&u) != cudaSuccess)
         return W4A16_ERR_CUDA;
-    return v ? W4A16_ERR_TIMEOUT : W4A16_OK;
+    return (v | u) ? W4A16_ERR_TIMEOUT : W4A16_OK;
 }
 
 }  // extern "C"

@@ -1,24 +1,28 @@
 // Prefill GEMM of the W4A16 layer on the 5th-generation tensor cores.
 //
-// Design (one CTA per SM, persistent over 128 x 256 output tiles):
+// Design (one CTA per SM, persistent over 256 x 128 output tiles):
 //
-//   warp 0      TMA producer: per 64-deep K step, the x tile [128 x 64]
-//               (128-byte swizzle) and the packed weight tile [8 words x 256]
-//               land in one stage of a shared-memory ring.
-//   warps 8-15  dequantise the packed tile ONCE into a [256 x 64] fp16/bf16
+//   warp 0      producer: per 64-deep K step, TMA brings the x tile [256 x 64]
+//               (128-byte swizzle) and the packed weight tile [8 words x 128];
+//               the warp's lanes stage the step's scales and zero-point words
+//               with cp.async (zero-filled outside N and K). All of it lands
+//               in one stage of a 4-deep ring and completes one mbarrier.
+//   warps 8-15  dequantise the packed tile ONCE into a [128 x 64] fp16/bf16
 //               operand tile in the canonical K-major 128-byte-swizzled layout
 //               the MMA reads: w = (q - z) * s, with (q - z) exact in 16-bit
 //               arithmetic and one rounding for the product. This is the
 //               cooperative shared tile of "ROCm KQuantGemmKWmmaQ4K/Q6K:
 //               redesign around a cooperative shared tile" (section "Confirmed
 //               mechanism"): the weight tile is loaded and dequantised once per
-//               CTA and every MMA of the tile consumes the same copy. As on
-//               "Add BF16xFP4 MoE GEMM stage1 kernel" (section "Technical
-//               Details"), weights are decoded in software before the MMA,
-//               which takes fp16/bf16 operands.
-//   warp 1      one thread issues tcgen05.mma (kind::f16, M=128, N=256, K=16)
-//               into an FP32 accumulator in tensor memory; two accumulators
-//               alternate so the epilogue of one tile overlaps the next.
+//               CTA and every MMA of the tile consumes the same copy -- here
+//               both 128-row halves of the x tile, so each dequantised weight
+//               feeds 256 rows of x. As on "Add BF16xFP4 MoE GEMM stage1
+//               kernel" (section "Technical Details"), weights are decoded in
+//               software before the MMA, which takes fp16/bf16 operands.
+//   warp 1      one thread issues tcgen05.mma (kind::f16, M=128, N=128, K=16,
+//               twice per K slice: one per M half) into FP32 accumulators in
+//               tensor memory; two 256-column accumulators alternate so the
+//               epilogue of one tile overlaps the MMAs of the next.
 //   warps 4-7   epilogue: tcgen05.ld from tensor memory, round to the output
 //               dtype, predicated 16-byte stores (every store is guarded on
 //               both M and N, the lesson of the col_n_valid guard on the MoE
@@ -43,22 +47,26 @@ __device__ unsigned int g_device_error = 0;
 
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64;
+constexpr int BM = 256, BN = 128, BK = 64;
+constexpr int UM = 128;                  // rows per tcgen05.mma: a tile is two M halves
 constexpr int kLoadStages = 4;           // x tile + packed weights + scales + zero-points
 constexpr int kBStages = 3;              // dequantised operand tiles
 constexpr int kThreads = 512;
 constexpr int kEpiWarp0 = 4;             // warps 4..7
-constexpr int kDeqWarp0 = 8;             // warps 8..15
-constexpr int kDeqWarps = 8;             // one dequant thread per column of the tile
-constexpr uint32_t kABytes = BM * BK * 2;            // 16 KB
-constexpr uint32_t kWBytes = (BK / 8) * BN * 4;      //  8 KB
-constexpr uint32_t kSBytes = 2 * BN * 2;             //  1 KB: scales of the two 32-row halves of a step
-constexpr uint32_t kZBytes = 2 * (BN / 8) * 4;       // 256 B: zero-point words of the two halves
+constexpr int kDeqWarp0 = 8;             // warps 8..15: two threads per column of the tile
+constexpr int kDeqWarps = 8;
+constexpr uint32_t kABytes = BM * BK * 2;            // 32 KB
+constexpr uint32_t kWBytes = (BK / 8) * BN * 4;      //  4 KB
+constexpr uint32_t kSBytes = 2 * BN * 2;             // 512 B: scales of the two 32-row halves of a step
+constexpr uint32_t kZBytes = 2 * (BN / 8) * 4;       // 128 B: zero-point words of the two halves
 constexpr uint32_t kLoadStageBytes = (kABytes + kWBytes + kSBytes + kZBytes + 1023) & ~1023u;
-constexpr uint32_t kBBytes = BN * BK * 2;            // 32 KB
-constexpr uint32_t kTmemCols = 2 * BN;               // two accumulators
+constexpr uint32_t kBBytes = BN * BK * 2;            // 16 KB
+constexpr uint32_t kAccCols = 2 * BN;                // one accumulator: two M halves side by side
+constexpr uint32_t kTmemCols = 2 * kAccCols;         // two accumulators
+constexpr uint32_t kSuspendNs = 20000;
 constexpr unsigned long long kWaitLimitCycles = 4000000000ull;   // ~2 s at 2 GHz
 constexpr unsigned int kErrTimeout = 9u;
+static_assert(kTmemCols == 512, "tensor memory budget");
 
 struct __align__(8) Barriers {
     uint64_t lfull[kLoadStages];    // x + weights (TMA bytes) and scales/zero-points (cp.async) landed
@@ -77,18 +85,17 @@ constexpr size_t kSmemBytes =
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
 // Bounded wait: false if the wait ran out (or another role already gave up).
+// The thread sleeps inside try_wait while the phase is incomplete.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = clock64();
-    for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 15u) == 0) {
-            if (*abort) return false;
-            if (clock64() - t0 > kWaitLimitCycles) {
-                *abort = 1;
-                atomicOr(&g_device_error, 1u << kErrTimeout);
-                return false;
-            }
+    for (;;) {
+        if (mbar_try_wait_suspend(bar, parity, kSuspendNs)) return true;
+        if (*abort) return false;
+        if (clock64() - t0 > kWaitLimitCycles) {
+            *abort = 1;
+            atomicOr(&g_device_error, 1u << kErrTimeout);
+            return false;
         }
     }
 }
@@ -157,7 +164,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
     Barriers* bars = reinterpret_cast<Barriers*>(bsmem + kBStages * kBBytes);
     const uint32_t smem_base = smem_u32(smem);
     const uint32_t bsmem_base = smem_u32(bsmem);
-    // load stage s: [x tile | packed weights | scales | zero-point words]
+    // load stage s: [x tile (two 128-row halves) | packed weights | scales | zero-point words]
     auto ld_a = [&](int s) { return smem_base + s * kLoadStageBytes; };
     auto ld_w = [&](int s) { return smem + s * kLoadStageBytes + kABytes; };
     auto ld_s = [&](int s) { return smem + s * kLoadStageBytes + kABytes + kWBytes; };
@@ -198,9 +205,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer warp
-        // lane l stages the scales of columns [8l, 8l+8) and their zero-point word
-        // with cp.async (zero-filled outside N and K); lane 0 then issues the TMA
-        // copies of the x tile and the packed weight tile.
+        // lane l stages, for 32-row half (l >> 4) of the step, the scales of the
+        // 8 columns [8(l&15), 8(l&15)+8) and their zero-point word with cp.async
+        // (zero-filled outside N and K); lane 0 then issues the TMA copies of the
+        // x tile and the packed weight tile.
+        const int half = lane >> 4, sub = lane & 15;
         int stage = 0;
         uint32_t phase = 0;
         uint32_t issued_parity[kLoadStages];
@@ -209,20 +218,17 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
         bool ok = true;
         for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
             const int m_blk = t % num_m, n_blk = t / num_m;
-            const int n = n_blk * BN + 8 * lane;
+            const int n = n_blk * BN + 8 * sub;
             for (int kt = 0; kt < kt_total; ++kt) {
                 if (!warp_wait_bar(smem_u32(&bars->lempty[stage]), phase ^ 1u, abort_flag, lane)) { ok = false; break; }
                 const uint32_t fb = smem_u32(&bars->lfull[stage]);
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    const int grp = (kt * BK + half * (BK / 2)) / g;
-                    const bool valid = n < N && grp < groups;
-                    const size_t so = valid ? static_cast<size_t>(grp) * N + n : 0;
-                    cp_async_16(smem_u32(ld_s(stage)) + half * (BN * 2) + 16 * lane, sc + so, valid ? 16u : 0u);
-                    if constexpr (!kSym) {
-                        const size_t zo = valid ? static_cast<size_t>(grp) * (N >> 3) + (n >> 3) : 0;
-                        cp_async_4(smem_u32(ld_z(stage)) + half * (BN / 8) * 4 + 4 * lane, qz + zo, valid ? 4u : 0u);
-                    }
+                const int grp = (kt * BK + half * (BK / 2)) / g;
+                const bool valid = n < N && grp < groups;
+                const size_t so = valid ? static_cast<size_t>(grp) * N + n : 0;
+                cp_async_16(smem_u32(ld_s(stage)) + half * (BN * 2) + 16 * sub, sc + so, valid ? 16u : 0u);
+                if constexpr (!kSym) {
+                    const size_t zo = valid ? static_cast<size_t>(grp) * (N >> 3) + (n >> 3) : 0;
+                    cp_async_4(smem_u32(ld_z(stage)) + half * (BN / 8) * 4 + 4 * sub, qz + zo, valid ? 4u : 0u);
                 }
                 cp_async_mbar_arrive(fb);
                 __syncwarp();
@@ -249,7 +255,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t kIdesc = umma_idesc_f16(BM, BN, kBf16);
+            constexpr uint32_t kIdesc = umma_idesc_f16(UM, BN, kBf16);
             int ls = 0, bs = 0;
             uint32_t lph = 0, bph = 0;
             int acc = 0;
@@ -258,7 +264,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
             for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
                 if (!wait_bar(smem_u32(&bars->tempty[acc]), acc_phase ^ 1u, abort_flag)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kAccCols);
                 for (int kt = 0; kt < kt_total; ++kt) {
                     if (!wait_bar(smem_u32(&bars->lfull[ls]), lph, abort_flag) ||
                         !wait_bar(smem_u32(&bars->bfull[bs]), bph, abort_flag)) {
@@ -266,12 +272,16 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t adesc = sw128_kmajor_desc(ld_a(ls));
                     const uint64_t bdesc = sw128_kmajor_desc(op_b(bs));
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk) {
-                        // advance 16 elements (32 bytes) along K inside the swizzle atom
-                        umma_f16(d_tmem, adesc + 2u * kk, bdesc + 2u * kk, kIdesc, (kt | kk) != 0);
+                    for (int h = 0; h < 2; ++h) {
+                        // M half h: rows [128h, 128h + 128) of the x tile -> accumulator columns [128h, 128h + 128)
+                        const uint64_t adesc = sw128_kmajor_desc(ld_a(ls) + h * (UM * BK * 2));
+#pragma unroll
+                        for (int kk = 0; kk < BK / 16; ++kk) {
+                            // advance 16 elements (32 bytes) along K inside the swizzle atom
+                            umma_f16(d_tmem + h * BN, adesc + 2u * kk, bdesc + 2u * kk, kIdesc, (kt | kk) != 0);
+                        }
                     }
                     umma_commit(smem_u32(&bars->lempty[ls]));
                     umma_commit(smem_u32(&bars->bempty[bs]));
@@ -291,33 +301,35 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
     } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 4) {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;                 // tensor-memory lane quarter of this warp
-        const int row = q * 32 + lane;
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
             const int m_blk = t % num_m, n_blk = t / num_m;
             if (!warp_wait_bar(smem_u32(&bars->tfull[acc]), acc_phase, abort_flag, lane)) break;
             tc_fence_after();
-            const int m = m_blk * BM + row;
-            uint16_t* yrow = y + static_cast<size_t>(m) * N;
 #pragma unroll 1
-            for (int ch = 0; ch < BN / 32; ++ch) {
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                                       static_cast<uint32_t>(acc * BN + ch * 32),
-                                   r);
-                tmem_wait_ld();
-                const int n = n_blk * BN + ch * 32;
-                if (m < M) {
+            for (int h = 0; h < 2; ++h) {
+                const int m = m_blk * BM + h * UM + q * 32 + lane;
+                uint16_t* yrow = y + static_cast<size_t>(m) * N;
+#pragma unroll 1
+                for (int ch = 0; ch < BN / 32; ++ch) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                           static_cast<uint32_t>(acc * kAccCols + h * BN + ch * 32),
+                                       r);
+                    tmem_wait_ld();
+                    const int n = n_blk * BN + ch * 32;
+                    if (m < M) {
 #pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        if (n + 8 * v < N) {
-                            uint4 o;
-                            o.x = Deq<kBf16>::pack2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
-                            o.y = Deq<kBf16>::pack2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
-                            o.z = Deq<kBf16>::pack2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
-                            o.w = Deq<kBf16>::pack2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
-                            *reinterpret_cast<uint4*>(yrow + n + 8 * v) = o;
+                        for (int v = 0; v < 4; ++v) {
+                            if (n + 8 * v < N) {
+                                uint4 o;
+                                o.x = Deq<kBf16>::pack2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
+                                o.y = Deq<kBf16>::pack2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
+                                o.z = Deq<kBf16>::pack2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
+                                o.w = Deq<kBf16>::pack2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
+                                *reinterpret_cast<uint4*>(yrow + n + 8 * v) = o;
+                            }
                         }
                     }
                 }
@@ -329,7 +341,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
         }
     } else if (warp >= kDeqWarp0) {
         // ------------------------------------------------------------ dequantisers
-        const int d = threadIdx.x - kDeqWarp0 * 32;    // column of the tile, 0..255
+        const int td = threadIdx.x - kDeqWarp0 * 32;   // 0..255
+        const int d = td & (BN - 1);                     // column of the tile
+        const int half = td >> 7;                        // 32-row half of the step: words 4*half .. 4*half+3
         int ls = 0, bs = 0;
         uint32_t lph = 0, bph = 0;
         bool ok = true;
@@ -344,32 +358,28 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
                 const uint16_t* st = reinterpret_cast<const uint16_t*>(ld_s(ls));
                 const uint32_t* zt = reinterpret_cast<const uint32_t*>(ld_z(ls));
                 const uint32_t b_row = op_b(bs) + static_cast<uint32_t>(d) * 128u;
+                const uint32_t s16 = st[half * BN + d];
+                const uint32_t z4 = kSym ? 8u : ((zt[half * (BN / 8) + (d >> 3)] >> (4 * (d & 7))) & 0xFu);
+                const uint32_t ss = s16 | (s16 << 16);
+                const uint32_t zz = Deq<kBf16>::kMagic | z4 | (z4 << 16);
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    // words c = 4*half .. 4*half+3 cover K rows [32*half, 32*half + 32) of the step
-                    const uint32_t s16 = st[half * BN + d];
-                    const uint32_t z4 = kSym ? 8u : ((zt[half * (BN / 8) + (d >> 3)] >> (4 * (d & 7))) & 0xFu);
-                    const uint32_t ss = s16 | (s16 << 16);
-                    const uint32_t zz = Deq<kBf16>::kMagic | z4 | (z4 << 16);
+                for (int cc = 0; cc < 4; ++cc) {
+                    const int c = half * 4 + cc;
+                    const uint32_t w = wt[c * BN + d];
+                    const uint32_t w4 = w >> 4;
+                    uint32_t o[4];
 #pragma unroll
-                    for (int cc = 0; cc < 4; ++cc) {
-                        const int c = half * 4 + cc;
-                        const uint32_t w = wt[c * BN + d];
-                        const uint32_t w4 = w >> 4;
-                        uint32_t o[4];
-#pragma unroll
-                        for (int b = 0; b < 4; ++b) {
-                            // byte b of w -> low half, byte b of (w >> 4) -> high half:
-                            // halves (magic + q[8c + 2b], magic + q[8c + 2b + 1])
-                            const uint32_t h = and_or(prmt(w, w4, static_cast<uint32_t>(b | ((4 + b) << 8))),
-                                                      0x000F000Fu, Deq<kBf16>::kMagic);
-                            o[b] = Deq<kBf16>::mul2(Deq<kBf16>::sub2(h, zz), ss);
-                        }
-                        const uint32_t dst = b_row + (static_cast<uint32_t>(c ^ (d & 7)) << 4);
-                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(o[0]), "r"(o[1]),
-                                     "r"(o[2]), "r"(o[3])
-                                     : "memory");
+                    for (int b = 0; b < 4; ++b) {
+                        // byte b of w -> low half, byte b of (w >> 4) -> high half:
+                        // halves (magic + q[8c + 2b], magic + q[8c + 2b + 1])
+                        const uint32_t h = and_or(prmt(w, w4, static_cast<uint32_t>(b | ((4 + b) << 8))),
+                                                  0x000F000Fu, Deq<kBf16>::kMagic);
+                        o[b] = Deq<kBf16>::mul2(Deq<kBf16>::sub2(h, zz), ss);
                     }
+                    const uint32_t dst = b_row + (static_cast<uint32_t>(c ^ (d & 7)) << 4);
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(o[0]), "r"(o[1]),
+                                 "r"(o[2]), "r"(o[3])
+                                 : "memory");
                 }
                 fence_proxy_async_smem();
                 __syncwarp();

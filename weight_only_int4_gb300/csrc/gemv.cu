@@ -12,11 +12,15 @@
 //     block first. A persistent grid of exactly two CTAs per SM takes equal
 //     contiguous ranges of items ("stream-K"), so every SM streams the same
 //     number of bytes whatever N and K are.
-//   * Inside a CTA the 8 warps take the chunks of the current column block in
-//     turn. A lane owns COLS adjacent columns and loads, per chunk, 4 rows x
-//     COLS packed words with 128-bit non-allocating loads plus its scales and
-//     zero-point word; the next chunk's loads are issued before the current
-//     chunk is converted (register double buffer), so memory and ALU overlap.
+//   * Inside a CTA the warps take the chunks of the current column block in
+//     turn. Each warp streams its chunks through its own kStages-deep ring in
+//     shared memory: one lane issues bulk asynchronous copies (TMA, completion
+//     counted in bytes on the stage's mbarrier) of the chunk's 4 packed word
+//     rows, its scales, its packed zero-points and the x slice, kStages chunks
+//     ahead of the one being converted, so memory and ALU overlap with about
+//     kWarps * (kStages - 1) chunks in flight per CTA and no load instructions
+//     on the lanes. A lane owns COLS columns in groups of 4 adjacent columns,
+//     32 groups apart, so all its shared-memory reads are bank-conflict free.
 //   * Nibbles become 16-bit floats by the exponent-bias trick: OR a nibble into
 //     the mantissa of 1024.0 (fp16) or 128.0 (bf16). For M <= 4 the zero-point
 //     is applied once per chunk through
@@ -36,14 +40,27 @@
 #include <algorithm>
 
 namespace w4a16 {
+
+__device__ unsigned int g_gemv_error = 0;
+
 namespace {
 
-constexpr int kWarps = 8;
+// Warps per CTA and depth of each warp's shared-memory ring.
+#ifndef W4A16_GEMV_WARPS
+#define W4A16_GEMV_WARPS 16
+#endif
+#ifndef W4A16_GEMV_STAGES
+#define W4A16_GEMV_STAGES 2
+#endif
+constexpr int kWarps = W4A16_GEMV_WARPS;
+constexpr int kStages = W4A16_GEMV_STAGES;
 constexpr int kThreads = kWarps * 32;
 constexpr int kChunk = 32;            // rows of K per chunk
 constexpr int kRowsPerChunk = 4;      // packed word rows per chunk
 constexpr int kFactMaxM = 4;          // zero-point by chunk sums up to this M
 constexpr size_t kXsumSmemLimit = 32 * 1024;
+constexpr unsigned long long kWaitLimitCycles = 4000000000ull;   // ~2 s at 2 GHz
+constexpr unsigned int kErrTimeout = 9u;
 
 template <bool kBf16>
 struct Act;
@@ -72,66 +89,72 @@ struct Act<true> {
     }
 };
 
-__device__ __forceinline__ uint4 ld_stream_v4(const uint32_t* p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
-__device__ __forceinline__ uint2 ld_stream_v2(const uint32_t* p) {
-    uint2 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
-    return v;
-}
-__device__ __forceinline__ uint32_t ld_stream_v1(const uint32_t* p) {
-    uint32_t v;
-    asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
-    return v;
+// One stage of a warp's ring holds, for one 32-row chunk of K and one column
+// block of CB = 32 * COLS columns: the 4 packed word rows [4][CB], the scales
+// [CB], the zero-point words [CB / 8] and the x slice [M][32]. A lane owns
+// COLS columns in groups of W = min(COLS, 4) adjacent columns, one group per
+// 32*W columns, so every lane-wise shared-memory read of a warp covers
+// contiguous bytes (no bank conflicts).
+template <int COLS, int MT>
+struct Stage {
+    static constexpr int CB = 32 * COLS;
+    static constexpr int W = COLS < 4 ? COLS : 4;         // columns per group
+    static constexpr int G = COLS / W;                    // groups per lane
+    static constexpr int kQ = 0;                          // [4][CB] uint32
+    static constexpr int kS = kQ + kRowsPerChunk * CB * 4;   // [CB] 16-bit scales
+    static constexpr int kZ = kS + CB * 2;                // [CB / 8] uint32
+    static constexpr int kX = kZ + CB / 2;                // [MT][32] 16-bit x
+    static constexpr int kBytes = kX + MT * kChunk * 2;
+    static_assert(kS % 16 == 0 && kZ % 16 == 0 && kX % 16 == 0 && kBytes % 16 == 0, "16-byte aligned blocks");
+    __device__ static int col(int lane, int gi, int u) { return gi * 32 * W + lane * W + u; }
+};
+
+__host__ __device__ constexpr int stage_bytes(int cols, int mt) {
+    return 32 * cols * (kRowsPerChunk * 4 + 2) + 32 * cols / 2 + mt * kChunk * 2;
 }
 
-template <int COLS>
-__device__ __forceinline__ void load_words(const uint32_t* p, uint32_t (&v)[COLS]) {
-    if constexpr (COLS == 8) {
-        const uint4 a = ld_stream_v4(p), b = ld_stream_v4(p + 4);
-        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-    } else if constexpr (COLS == 4) {
-        const uint4 a = ld_stream_v4(p);
-        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-    } else if constexpr (COLS == 2) {
-        const uint2 a = ld_stream_v2(p);
-        v[0] = a.x; v[1] = a.y;
-    } else {
-        v[0] = ld_stream_v1(p);
+template <int BYTES>
+__device__ __forceinline__ void lds(uint32_t addr, uint32_t (&v)[(BYTES + 3) / 4]) {
+    if constexpr (BYTES == 16)
+        asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]) : "r"(addr));
+    else if constexpr (BYTES == 8)
+        asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v[0]), "=r"(v[1]) : "r"(addr));
+    else if constexpr (BYTES == 4)
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v[0]) : "r"(addr));
+    else {
+        uint16_t h;
+        asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h) : "r"(addr));
+        v[0] = h;
     }
 }
 
-// COLS 16-bit scales packed two per word (SW words; the last half unused when COLS == 1).
-template <int COLS>
-struct ScaleWords {
-    static constexpr int SW = (COLS + 1) / 2;
-};
-template <int COLS>
-__device__ __forceinline__ void load_scales(const uint16_t* p, uint32_t (&v)[ScaleWords<COLS>::SW]) {
-    if constexpr (COLS == 8) {
-        const uint4 a = __ldg(reinterpret_cast<const uint4*>(p));
-        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-    } else if constexpr (COLS == 4) {
-        const uint2 a = __ldg(reinterpret_cast<const uint2*>(p));
-        v[0] = a.x; v[1] = a.y;
-    } else if constexpr (COLS == 2) {
-        v[0] = __ldg(reinterpret_cast<const uint32_t*>(p));
-    } else {
-        v[0] = __ldg(p);
-    }
+__device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
 }
 
-template <int COLS>
-struct ChunkRegs {
-    uint32_t q[kRowsPerChunk][COLS];
-    uint32_t s[ScaleWords<COLS>::SW];
-    uint32_t z;
-};
+// Lane 0 waits, bounded (about two seconds), sleeping in try_wait; then every
+// lane observes the completed phase itself.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int lane) {
+    int ok = 1;
+    if (lane == 0 && !mbar_try_wait(bar, parity)) {
+        const unsigned long long t0 = clock64();
+        while (!mbar_try_wait_suspend(bar, parity, 20000)) {
+            if (clock64() - t0 > kWaitLimitCycles) {
+                atomicOr(&g_gemv_error, 1u << kErrTimeout);
+                ok = 0;
+                break;
+            }
+        }
+    }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (ok && lane != 0) {
+        for (uint32_t i = 0; !mbar_try_wait(bar, parity) && i < (1u << 20); ++i) {
+        }
+    }
+    return ok != 0;
+}
 
 struct GemvArgs {
     const uint16_t* x;
@@ -146,29 +169,47 @@ struct GemvArgs {
     long long items;      // n_cb * chunks
 };
 
+// Byte offsets inside dynamic shared memory: warp partials | chunk sums of x | barriers | rings.
+__host__ __device__ constexpr uint32_t xsum_offset(int live_per_warp) { return kWarps * live_per_warp * 4; }
+__host__ __device__ constexpr uint32_t bar_offset(int live_per_warp, int xsum_entries) {
+    return (xsum_offset(live_per_warp) + xsum_entries * 8 + 15) & ~15u;
+}
+__host__ __device__ constexpr uint32_t ring_offset(int live_per_warp, int xsum_entries) {
+    return (bar_offset(live_per_warp, xsum_entries) + kWarps * kStages * 8 + 127) & ~127u;
+}
+
 // First CTA whose item range contains item i (ranges are [b*T/G, (b+1)*T/G)).
 __device__ __forceinline__ int owner_cta(long long i, long long T, int G) {
     return static_cast<int>(((i + 1) * G - 1) / T);
 }
 __device__ __forceinline__ long long range_start(int b, long long T, int G) { return (long long)b * T / G; }
 
-template <bool kBf16, int MT, int COLS, bool kSym, bool kFact>
-__global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
+template <bool kBf16, int MT, int COLS, bool kSym, bool kFact, bool kZBulk>
+__global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvArgs a) {
     using A = Act<kBf16>;
-    constexpr int CB = 32 * COLS;
+    using St = Stage<COLS, MT>;
+    constexpr int CB = St::CB;
     constexpr int E = MT * CB;
+    constexpr int W = St::W, G = St::G;
     constexpr bool kTwoFamilies = kFact && !kBf16;   // fp16: nibbles at bits 0-3 and 4-7 of a half
-    extern __shared__ float smem[];
-    float* red = smem;                          // [kWarps][E]
-    float2* xsum = reinterpret_cast<float2*>(smem + kWarps * E);   // [M][chunks]: (offset, sum x)
+    extern __shared__ __align__(128) uint8_t smem[];
     __shared__ int s_last;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int M = a.M, N = a.N, K = a.K, g = a.g, chunks = a.chunks;
     const long long T = a.items;
-    const int G = gridDim.x, b = blockIdx.x;
-    const long long i_begin = range_start(b, T, G), i_end = range_start(b + 1, T, G);
+    const int Gd = gridDim.x, b = blockIdx.x;
+    const long long i_begin = range_start(b, T, Gd), i_end = range_start(b + 1, T, Gd);
+    const int xs_entries = kFact ? M * chunks : 0;
+    float* red = reinterpret_cast<float*>(smem);                                   // [kWarps][E]
+    float2* xsum = reinterpret_cast<float2*>(smem + xsum_offset(E));               // [M][chunks]
+    const uint32_t bars = smem_u32(smem) + bar_offset(E, xs_entries) + warp * kStages * 8;
+    const uint32_t ring = smem_u32(smem) + ring_offset(E, xs_entries) + warp * kStages * St::kBytes;
 
+    if (lane == 0) {
+        for (int st = 0; st < kStages; ++st) mbar_init(bars + 8 * st, 1);
+        fence_mbar_init();
+    }
     if constexpr (kFact) {
         // per (row, chunk): sum of x over the chunk, and the offset the magic bias adds
         for (int p = threadIdx.x; p < M * chunks; p += kThreads) {
@@ -188,16 +229,18 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
             const float off = kTwoFamilies ? (A::kMagicF * se + (A::kMagicF / 16.f) * so) : A::kMagicF * (se + so);
             xsum[p] = make_float2(off, se + so);
         }
-        __syncthreads();
     }
+    __syncthreads();
+
+    uint32_t phase_bits = 0;   // parity of the next completion of each stage's barrier
+    bool ok = true;
 
     for (long long it = i_begin; it < i_end;) {
         const int cb = static_cast<int>(it / chunks);
         const int c0 = static_cast<int>(it - static_cast<long long>(cb) * chunks);
         const int c1 = static_cast<int>(std::min<long long>(chunks, c0 + (i_end - it)));
-        const int n0 = cb * CB + lane * COLS;
-        const bool col_ok = n0 < N;               // N % 8 == 0 and COLS | 8: all COLS columns valid
-        const int zshift = 4 * (n0 & 7);
+        const int ncols = std::min(CB, N - cb * CB);
+        const int nj = ok ? (c1 - c0 - warp + kWarps - 1) / kWarps : 0;   // this warp's chunks
 
         float yacc[MT][COLS];
 #pragma unroll
@@ -205,16 +248,55 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
 #pragma unroll
             for (int j = 0; j < COLS; ++j) yacc[m][j] = 0.f;
 
-        auto load = [&](ChunkRegs<COLS>& r, int c) {
-            const uint32_t* p = a.qw + static_cast<size_t>(c) * kRowsPerChunk * N + n0;
-#pragma unroll
-            for (int i = 0; i < kRowsPerChunk; ++i) load_words<COLS>(p + static_cast<size_t>(i) * N, r.q[i]);
+        // lane 0: bring chunk c of this column block into stage st
+        auto issue = [&](int st, int c) {
+            const uint32_t base = ring + st * St::kBytes, bar = bars + 8 * st;
             const int t = (c * kChunk) / g;
-            load_scales<COLS>(a.sc + static_cast<size_t>(t) * N + n0, r.s);
-            if constexpr (!kSym) r.z = __ldg(a.qz + static_cast<size_t>(t) * (N >> 3) + (n0 >> 3));
+            const uint32_t bytes = ncols * (kRowsPerChunk * 4 + 2) + (kZBulk ? ncols / 2 : 0) + M * kChunk * 2;
+            mbar_arrive_expect_tx(bar, bytes);
+            const uint32_t* q = a.qw + static_cast<size_t>(c) * kRowsPerChunk * N + static_cast<size_t>(cb) * CB;
+#pragma unroll
+            for (int i = 0; i < kRowsPerChunk; ++i)
+                bulk_copy(base + St::kQ + i * CB * 4, q + static_cast<size_t>(i) * N, ncols * 4, bar);
+            bulk_copy(base + St::kS, a.sc + static_cast<size_t>(t) * N + static_cast<size_t>(cb) * CB, ncols * 2, bar);
+            if constexpr (kZBulk)
+                bulk_copy(base + St::kZ, a.qz + static_cast<size_t>(t) * (N >> 3) + static_cast<size_t>(cb) * (CB / 8),
+                          ncols / 2, bar);
+            for (int m = 0; m < M; ++m)
+                bulk_copy(base + St::kX + m * kChunk * 2, a.x + static_cast<size_t>(m) * K + c * kChunk, kChunk * 2, bar);
         };
 
-        auto compute = [&](const ChunkRegs<COLS>& r, int c) {
+        auto compute = [&](int st, int c) {
+            const uint32_t base = ring + st * St::kBytes;
+            // scales and zero-points of the lane's columns
+            uint32_t sw[G][(2 * W + 3) / 4], zw[G];
+#pragma unroll
+            for (int gi = 0; gi < G; ++gi) {
+                const int c0l = St::col(lane, gi, 0);
+                lds<2 * W>(base + St::kS + c0l * 2, sw[gi]);
+                if constexpr (!kSym) {
+                    if constexpr (kZBulk) {
+                        uint32_t v[1];
+                        lds<4>(base + St::kZ + (c0l >> 3) * 4, v);
+                        zw[gi] = v[0];
+                    } else {
+                        const int t = (c * kChunk) / g;
+                        const int n = cb * CB + c0l;
+                        zw[gi] = n < N ? __ldg(a.qz + static_cast<size_t>(t) * (N >> 3) + (n >> 3)) : 0u;
+                    }
+                } else {
+                    zw[gi] = 0u;
+                }
+            }
+            auto zval = [&](int j) -> uint32_t {
+                const int gi = j / W, u = j % W;
+                return kSym ? 8u : ((zw[gi] >> (4 * ((St::col(lane, gi, 0) & 7) + u))) & 0xFu);
+            };
+            auto sval = [&](int j) -> float {
+                const int gi = j / W, u = j % W;
+                return A::to_float(static_cast<uint16_t>(sw[gi][u / 2] >> (16 * (u & 1))));
+            };
+
             float acc[MT][COLS], acc2[kTwoFamilies ? MT : 1][kTwoFamilies ? COLS : 1];
 #pragma unroll
             for (int m = 0; m < MT; ++m)
@@ -230,17 +312,25 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
             if constexpr (!kFact) {
 #pragma unroll
                 for (int j = 0; j < COLS; ++j) {
-                    const uint32_t z = kSym ? 8u : ((r.z >> (zshift + 4 * j)) & 0xFu);
+                    const uint32_t z = zval(j);
                     zz[j] = A::kMagic | z | (z << 16);
                 }
             }
 #pragma unroll
             for (int i = 0; i < kRowsPerChunk; ++i) {
+                uint32_t q[COLS];
+#pragma unroll
+                for (int gi = 0; gi < G; ++gi) {
+                    uint32_t v[W];
+                    lds<4 * W>(base + St::kQ + i * CB * 4 + St::col(lane, gi, 0) * 4, v);
+#pragma unroll
+                    for (int u = 0; u < W; ++u) q[gi * W + u] = v[u];
+                }
                 // nibble pairs of this word row for every column, converted once ...
                 uint32_t h[COLS][4];
 #pragma unroll
                 for (int j = 0; j < COLS; ++j) {
-                    const uint32_t w = r.q[i][j];
+                    const uint32_t w = q[j];
                     if constexpr (kTwoFamilies) {
                         // (1024 + q[k], 1024 + q[k+4]), (1024 + 16 q[k+1], 1024 + 16 q[k+5]),
                         // (1024 + q[k+2], 1024 + q[k+6]), (1024 + 16 q[k+3], 1024 + 16 q[k+7])
@@ -259,32 +349,31 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
                     }
                 }
                 // ... then streamed against one row of x at a time
-                const int k = c * kChunk + i * 8;
 #pragma unroll
                 for (int m = 0; m < MT; ++m) {
-                    const uint4 xv = (m < M) ? __ldg(reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(m) * K + k))
-                                             : make_uint4(0u, 0u, 0u, 0u);
+                    uint32_t xw[4] = {0u, 0u, 0u, 0u};
+                    if (m < M) lds<16>(base + St::kX + m * kChunk * 2 + i * 16, xw);
 #pragma unroll
                     for (int j = 0; j < COLS; ++j) {
                         if constexpr (kTwoFamilies) {
-                            acc[m][j] = fma_mixed<false, 0, 0>(h[j][0], xv.x, acc[m][j]);
-                            acc[m][j] = fma_mixed<false, 1, 0>(h[j][0], xv.z, acc[m][j]);
-                            acc[m][j] = fma_mixed<false, 0, 0>(h[j][2], xv.y, acc[m][j]);
-                            acc[m][j] = fma_mixed<false, 1, 0>(h[j][2], xv.w, acc[m][j]);
-                            acc2[m][j] = fma_mixed<false, 0, 1>(h[j][1], xv.x, acc2[m][j]);
-                            acc2[m][j] = fma_mixed<false, 1, 1>(h[j][1], xv.z, acc2[m][j]);
-                            acc2[m][j] = fma_mixed<false, 0, 1>(h[j][3], xv.y, acc2[m][j]);
-                            acc2[m][j] = fma_mixed<false, 1, 1>(h[j][3], xv.w, acc2[m][j]);
+                            acc[m][j] = fma_mixed<false, 0, 0>(h[j][0], xw[0], acc[m][j]);
+                            acc[m][j] = fma_mixed<false, 1, 0>(h[j][0], xw[2], acc[m][j]);
+                            acc[m][j] = fma_mixed<false, 0, 0>(h[j][2], xw[1], acc[m][j]);
+                            acc[m][j] = fma_mixed<false, 1, 0>(h[j][2], xw[3], acc[m][j]);
+                            acc2[m][j] = fma_mixed<false, 0, 1>(h[j][1], xw[0], acc2[m][j]);
+                            acc2[m][j] = fma_mixed<false, 1, 1>(h[j][1], xw[2], acc2[m][j]);
+                            acc2[m][j] = fma_mixed<false, 0, 1>(h[j][3], xw[1], acc2[m][j]);
+                            acc2[m][j] = fma_mixed<false, 1, 1>(h[j][3], xw[3], acc2[m][j]);
                         } else {
                             // pair bb holds x[k+bb] (word bb/2 of x, half bb&1) and x[k+bb+4]
-                            acc[m][j] = fma_mixed<kBf16, 0, 0>(h[j][0], xv.x, acc[m][j]);
-                            acc[m][j] = fma_mixed<kBf16, 1, 0>(h[j][0], xv.z, acc[m][j]);
-                            acc[m][j] = fma_mixed<kBf16, 0, 1>(h[j][1], xv.x, acc[m][j]);
-                            acc[m][j] = fma_mixed<kBf16, 1, 1>(h[j][1], xv.z, acc[m][j]);
-                            acc[m][j] = fma_mixed<kBf16, 0, 0>(h[j][2], xv.y, acc[m][j]);
-                            acc[m][j] = fma_mixed<kBf16, 1, 0>(h[j][2], xv.w, acc[m][j]);
-                            acc[m][j] = fma_mixed<kBf16, 0, 1>(h[j][3], xv.y, acc[m][j]);
-                            acc[m][j] = fma_mixed<kBf16, 1, 1>(h[j][3], xv.w, acc[m][j]);
+                            acc[m][j] = fma_mixed<kBf16, 0, 0>(h[j][0], xw[0], acc[m][j]);
+                            acc[m][j] = fma_mixed<kBf16, 1, 0>(h[j][0], xw[2], acc[m][j]);
+                            acc[m][j] = fma_mixed<kBf16, 0, 1>(h[j][1], xw[0], acc[m][j]);
+                            acc[m][j] = fma_mixed<kBf16, 1, 1>(h[j][1], xw[2], acc[m][j]);
+                            acc[m][j] = fma_mixed<kBf16, 0, 0>(h[j][2], xw[1], acc[m][j]);
+                            acc[m][j] = fma_mixed<kBf16, 1, 0>(h[j][2], xw[3], acc[m][j]);
+                            acc[m][j] = fma_mixed<kBf16, 0, 1>(h[j][3], xw[1], acc[m][j]);
+                            acc[m][j] = fma_mixed<kBf16, 1, 1>(h[j][3], xw[3], acc[m][j]);
                         }
                     }
                 }
@@ -292,9 +381,9 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
             // scale (and, for kFact, zero-point) once per chunk, in FP32
 #pragma unroll
             for (int j = 0; j < COLS; ++j) {
-                const float s = A::to_float(static_cast<uint16_t>(r.s[j / 2] >> (16 * (j & 1))));
+                const float s = sval(j);
                 if constexpr (kFact) {
-                    const float zf = kSym ? 8.f : static_cast<float>((r.z >> (zshift + 4 * j)) & 0xFu);
+                    const float zf = static_cast<float>(zval(j));
 #pragma unroll
                     for (int m = 0; m < MT; ++m) {
                         const float2 os = (m < M) ? xsum[m * chunks + c] : make_float2(0.f, 0.f);
@@ -309,32 +398,35 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
             }
         };
 
-        if (col_ok) {
-            ChunkRegs<COLS> b0, b1;
-            int c = c0 + warp;
-            if (c < c1) load(b0, c);
-            for (; c < c1; c += 2 * kWarps) {
-                const int cn = c + kWarps;
-                if (cn < c1) load(b1, cn);
-                compute(b0, c);
-                const int cnn = cn + kWarps;
-                if (cnn < c1) load(b0, cnn);
-                if (cn < c1) compute(b1, cn);
+        // this warp's chunks c0 + warp + kWarps * j, through its kStages-deep ring
+        if (lane == 0)
+            for (int j = 0; j < kStages && j < nj; ++j) issue(j, c0 + warp + kWarps * j);
+        for (int j = 0; j < nj; ++j) {
+            const int st = j % kStages;
+            if (!warp_wait(bars + 8 * st, (phase_bits >> st) & 1u, lane)) {
+                ok = false;
+                break;
             }
+            phase_bits ^= 1u << st;
+            compute(st, c0 + warp + kWarps * j);
+            // every lane's reads of the stage precede the copy that refills it
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0 && j + kStages < nj) issue(st, c0 + warp + kWarps * (j + kStages));
         }
 
-        // partial sums of the 8 warps -> shared memory, reduced in warp order
+        // partial sums of the warps -> shared memory, reduced in warp order
 #pragma unroll
         for (int m = 0; m < MT; ++m)
 #pragma unroll
-            for (int j = 0; j < COLS; ++j) red[warp * E + m * CB + lane * COLS + j] = yacc[m][j];
+            for (int j = 0; j < COLS; ++j) red[warp * E + m * CB + St::col(lane, j / W, j % W)] = yacc[m][j];
         __syncthreads();
         const int EM = M * CB;                       // live entries: rows m < M
         for (int e = threadIdx.x; e < EM; e += kThreads) {
-            float s = red[e];
+            float sum = red[e];
 #pragma unroll
-            for (int w = 1; w < kWarps; ++w) s += red[w * E + e];
-            red[e] = s;
+            for (int w = 1; w < kWarps; ++w) sum += red[w * E + e];
+            red[e] = sum;
         }
 
         auto store_y = [&](int e, float v) {
@@ -352,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
             __threadfence();
             __syncthreads();
             const long long first = static_cast<long long>(cb) * chunks, last = first + chunks - 1;
-            const int b_lo = owner_cta(first, T, G), b_hi = owner_cta(last, T, G);
+            const int b_lo = owner_cta(first, T, Gd), b_hi = owner_cta(last, T, Gd);
             if (threadIdx.x == 0) {
                 const unsigned old = atomicAdd(a.tickets + cb, 1u);
                 s_last = (old == static_cast<unsigned>(b_hi - b_lo));
@@ -361,13 +453,13 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
             if (s_last) {
                 __threadfence();
                 for (int e = threadIdx.x; e < EM; e += kThreads) {
-                    float s = 0.f;
+                    float sum = 0.f;
                     for (int bb = b_lo; bb <= b_hi; ++bb) {
-                        const long long st = std::max(range_start(bb, T, G), first);
+                        const long long st = std::max(range_start(bb, T, Gd), first);
                         const int sl = (st > first) ? 0 : 1;
-                        s += __ldcg(a.partials + (static_cast<size_t>(bb) * 2 + sl) * EM + e);
+                        sum += __ldcg(a.partials + (static_cast<size_t>(bb) * 2 + sl) * EM + e);
                     }
-                    store_y(e, s);
+                    store_y(e, sum);
                 }
                 if (threadIdx.x == 0) a.tickets[cb] = 0u;
             }
@@ -377,13 +469,17 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
     }
 }
 
-template <bool kBf16, int MT, int COLS, bool kSym, bool kFact>
+template <bool kBf16, int MT, int COLS, bool kSym, bool kFact, bool kZBulk>
 cudaError_t launch_one(const GemvArgs& a, const GemvPlan& p, cudaStream_t s) {
-    auto kern = gemv_kernel<kBf16, MT, COLS, kSym, kFact>;
+    static_assert(Stage<COLS, MT>::kBytes == stage_bytes(COLS, MT), "stage layout");
+    auto kern = gemv_kernel<kBf16, MT, COLS, kSym, kFact, kZBulk>;
     const size_t smem = p.smem_bytes;
-    if (smem > 48 * 1024) {
+    static size_t configured[64] = {0};   // largest dynamic shared memory set, per device
+    const int dev = p.device;
+    if (smem > 48 * 1024 && (dev < 0 || dev >= 64 || configured[dev] < smem)) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) configured[dev] = smem;
     }
     kern<<<p.grid, kThreads, smem, s>>>(a);
     return cudaGetLastError();
@@ -391,7 +487,10 @@ cudaError_t launch_one(const GemvArgs& a, const GemvPlan& p, cudaStream_t s) {
 
 template <bool kBf16, int MT, int COLS, bool kFact>
 cudaError_t launch_sym(const GemvArgs& a, const GemvPlan& p, cudaStream_t s) {
-    return a.qz ? launch_one<kBf16, MT, COLS, false, kFact>(a, p, s) : launch_one<kBf16, MT, COLS, true, kFact>(a, p, s);
+    const bool zb = (a.N % 32) == 0;
+    if (!a.qz) return launch_one<kBf16, MT, COLS, true, kFact, false>(a, p, s);
+    return zb ? launch_one<kBf16, MT, COLS, false, kFact, true>(a, p, s)
+              : launch_one<kBf16, MT, COLS, false, kFact, false>(a, p, s);
 }
 
 template <bool kBf16>
@@ -437,18 +536,22 @@ GemvPlan plan_gemv(int M, int N, int K, int g, const DeviceProps& dp) {
     const int chunks = K / kChunk;
     const long long items = static_cast<long long>(p.n_cb) * chunks;
     p.items = items;
-    // two resident CTAs per SM, each with at least one chunk per warp
-    const long long want = 2LL * dp.sms;
-    p.grid = static_cast<int>(std::max<long long>(1, std::min<long long>(want, items / kWarps)));
     const size_t xsum_bytes = static_cast<size_t>(M) * chunks * sizeof(float2);
     p.fact = M <= kFactMaxM && xsum_bytes <= kXsumSmemLimit;
-    p.smem_bytes = static_cast<size_t>(kWarps) * p.mt * p.cb * sizeof(float) + (p.fact ? xsum_bytes : 0);
+    const int live = p.mt * p.cb;
+    p.smem_bytes = ring_offset(live, p.fact ? M * chunks : 0) +
+                   static_cast<size_t>(kWarps) * kStages * stage_bytes(p.cols, p.mt);
+    // as many CTAs per SM as shared memory allows (at most 2), each with at least one chunk per warp
+    const int per_sm = p.smem_bytes * 2 <= dp.smem_optin ? 2 : 1;
+    const long long want = static_cast<long long>(per_sm) * dp.sms;
+    p.grid = static_cast<int>(std::max<long long>(1, std::min<long long>(want, items / kWarps)));
     p.ticket_bytes = (static_cast<size_t>(p.n_cb) * sizeof(uint32_t) + 255) & ~size_t(255);
     // Partial slots first, in a region whose size depends only on the device
     // (M * columns-per-block <= kMaxLive for every row template), tickets after
     // it: calls of different shapes sharing one workspace never write partial
     // sums over one another's tickets.
     p.partial_bytes = partial_region_bytes(dp);
+    p.device = dp.device;
     return p;
 }
 
@@ -471,6 +574,18 @@ cudaError_t launch_gemv(const void* x, const uint32_t* qw, const void* sc, const
     a.chunks = K / kChunk;
     a.items = plan.items;
     return bf16 ? launch_dtype<true>(a, plan, s) : launch_dtype<false>(a, plan, s);
+}
+
+cudaError_t read_and_clear_gemv_error(uint32_t* out) {
+    uint32_t v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_gemv_error, sizeof(v));
+    if (e != cudaSuccess) return e;
+    if (v) {
+        const uint32_t zero = 0;
+        e = cudaMemcpyToSymbol(g_gemv_error, &zero, sizeof(zero));
+    }
+    *out = v;
+    return e;
 }
 
 }  // namespace w4a16

@@ -34,6 +34,7 @@ struct GemvPlan {
     size_t smem_bytes = 0;  // dynamic shared memory per CTA
     size_t ticket_bytes = 0;
     size_t partial_bytes = 0;
+    int device = -1;
 };
 
 GemvPlan plan_gemv(int M, int N, int K, int g, const DeviceProps& dp);
@@ -51,5 +52,7 @@ cudaError_t launch_gemm(const void* x, const uint32_t* qw, const void* sc, const
 
 // Read and clear the device-side error word of the GEMM pipeline (after a sync).
 cudaError_t read_and_clear_device_error(uint32_t* out, cudaStream_t s);
+// Read and clear the device-side error word of the GEMV rings (no sync).
+cudaError_t read_and_clear_gemv_error(uint32_t* out);
 
 }  // namespace w4a16
