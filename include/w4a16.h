@@ -155,6 +155,39 @@ w4a16_status w4a16_gemv(const void* x, const int32_t* qweight, const void* scale
                         w4a16_stream stream);
 
 /*
+ * w4a16_gemv_noalloc -- w4a16_gemv for callers that cannot allocate device
+ * memory. (No counterpart on the pages this library follows.)
+ *
+ * Some callers have no way to obtain scratch memory: a plugin loaded into a
+ * host program that owns every device allocation and hands plugins no
+ * allocator; a serving process that has already reserved all device memory
+ * for its own pools; a latency-critical loop where cudaMalloc, which can
+ * synchronise the device and take unbounded time, is not allowed. This entry
+ * point takes the same arguments as w4a16_gemv minus the workspace and uses a
+ * fixed 4 MiB scratch array compiled into the library instead. It calls no
+ * cudaMalloc, cudaFree or other allocating routine.
+ *
+ * - The array lives in every GPU that loads the library, until the process
+ *   exits.
+ * - The first call on a device looks up the array's device address once
+ *   (cudaGetSymbolAddress, with that device current); make that first call
+ *   before any stream capture on the device.
+ * - Every call on a device uses the same array and clears its ticket words
+ *   (an asynchronous memset on `stream`) before the kernel. Two calls that can
+ *   run at the same time on one device (different streams) race on the array
+ *   and give wrong results: serialise them.
+ * - A shape whose scratch (w4a16_workspace_bytes(W4A16_OP_GEMV, ...)) exceeds
+ *   4 MiB is rejected with W4A16_ERR_WORKSPACE; the partial-sum region takes
+ *   16 KB per SM and each column block a 4-byte ticket, so on a 152-SM GB300
+ *   this allows N up to about 13 million.
+ * Results are identical to w4a16_gemv's for the same inputs. Other errors as
+ * for w4a16_gemv.
+ */
+w4a16_status w4a16_gemv_noalloc(const void* x, const int32_t* qweight, const void* scales,
+                                const int32_t* qzeros, void* y, int64_t M, int64_t N, int64_t K,
+                                int64_t g, w4a16_dtype dt, w4a16_stream stream);
+
+/*
  * w4a16_gemm -- prefill path, any M >= 1 (built for M in the hundreds or
  * more; small M works but wastes most of a 128-row tile).
  *

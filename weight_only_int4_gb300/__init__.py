@@ -49,6 +49,7 @@ SIGNATURES = {
     "w4a16_workspace_bytes": (_SZ, [_INT, _I64, _I64, _I64, _I64]),
     "w4a16_gemv": (_INT, _LAYER_ARGS),
     "w4a16_gemm": (_INT, _LAYER_ARGS),
+    "w4a16_gemv_noalloc": (_INT, [_VP, _VP, _VP, _VP, _VP, _I64, _I64, _I64, _I64, _INT, _VP]),
     "w4a16_device_status": (_INT, [_VP]),
     "w4a16_status_string": (ctypes.c_char_p, [_INT]),
     "w4a16_abi_version": (_INT, []),

@@ -146,6 +146,26 @@ w4a16_status w4a16_gemv(const void* x, const int32_t* qweight, const void* scale
                                         dt == W4A16_BF16, plan, workspace, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+w4a16_status w4a16_gemv_noalloc(const void* x, const int32_t* qweight, const void* scales, const int32_t* qzeros,
+                                void* y, int64_t M, int64_t N, int64_t K, int64_t g, w4a16_dtype dt,
+                                w4a16_stream stream) {
+    w4a16_status st = check_layer_args(x, qweight, scales, qzeros, y, M, N, K, g, dt, 16);
+    if (st != W4A16_OK) return st;
+    DeviceProps dp;
+    if ((st = device_gate(&dp)) != W4A16_OK) return st;
+    const w4a16::GemvPlan plan = w4a16::plan_gemv((int)M, (int)N, (int)K, (int)g, dp);
+    if (w4a16::gemv_workspace_bytes(plan) > w4a16::kGemvNoAllocScratchBytes) return W4A16_ERR_WORKSPACE;
+    void* scratch = nullptr;
+    if (w4a16::gemv_noalloc_scratch(dp.device, &scratch) != cudaSuccess) return W4A16_ERR_CUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // the ticket words must start at zero; the partial sums are written before they are read
+    if (cudaMemsetAsync(static_cast<uint8_t*>(scratch) + plan.partial_bytes, 0, plan.ticket_bytes, s) != cudaSuccess)
+        return W4A16_ERR_CUDA;
+    return from_cuda(w4a16::launch_gemv(x, reinterpret_cast<const uint32_t*>(qweight), scales,
+                                        reinterpret_cast<const uint32_t*>(qzeros), y, (int)M, (int)N, (int)K, (int)g,
+                                        dt == W4A16_BF16, plan, scratch, s));
+}
+
 w4a16_status w4a16_gemm(const void* x, const int32_t* qweight, const void* scales, const int32_t* qzeros, void* y,
                         int64_t M, int64_t N, int64_t K, int64_t g, w4a16_dtype dt, void* workspace,
                         size_t workspace_bytes, w4a16_stream stream) {

@@ -38,6 +38,7 @@
 #include "ptx.cuh"
 
 #include <algorithm>
+#include <mutex>
 
 namespace w4a16 {
 
@@ -574,6 +575,33 @@ cudaError_t launch_gemv(const void* x, const uint32_t* qw, const void* sc, const
     a.chunks = K / kChunk;
     a.items = plan.items;
     return bf16 ? launch_dtype<true>(a, plan, s) : launch_dtype<false>(a, plan, s);
+}
+
+// ---------------------------------------------------------------------------
+// Built-in scratch for callers that cannot allocate device memory
+// ---------------------------------------------------------------------------
+// The GEMV's scratch (partial sums of column blocks shared by several CTAs,
+// then one ticket word per column block) normally comes from the caller's
+// workspace. This fixed array serves w4a16_gemv_noalloc instead. It is zero
+// when the module loads; every GEMV call leaves its ticket words at zero, and
+// w4a16_gemv_noalloc clears them before each launch as well.
+static __device__ __align__(256) uint8_t g_gemv_noalloc_scratch[kGemvNoAllocScratchBytes];
+
+cudaError_t gemv_noalloc_scratch(int device, void** ptr) {
+    static std::mutex mu;
+    static void* cache[64] = {nullptr};
+    if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!cache[device]) {
+        // host code may not use the array's name as an address: ask the runtime,
+        // with `device` current (the caller's current device)
+        void* p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_gemv_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        cache[device] = p;
+    }
+    *ptr = cache[device];
+    return cudaSuccess;
 }
 
 cudaError_t read_and_clear_gemv_error(uint32_t* out) {

@@ -47,6 +47,13 @@ cudaError_t launch_gemv(const void* x, const uint32_t* qw, const void* sc, const
                         int M, int N, int K, int g, bool bf16, const GemvPlan& plan, void* workspace,
                         cudaStream_t s);
 
+// Size of the GEMV's built-in scratch array (w4a16_gemv_noalloc).
+constexpr size_t kGemvNoAllocScratchBytes = size_t(4) << 20;
+
+// Device address of that array on `device` (which must be current); looked up
+// once per device and cached.
+cudaError_t gemv_noalloc_scratch(int device, void** ptr);
+
 cudaError_t launch_gemm(const void* x, const uint32_t* qw, const void* sc, const uint32_t* qz, void* y,
                         int M, int N, int K, int g, bool bf16, const DeviceProps& dp, cudaStream_t s);
 
