@@ -36,8 +36,10 @@
 //     and resets the ticket to zero for the next call.
 #include "internal.h"
 #include "ptx.cuh"
+#include "tmap.h"
 
 #include <algorithm>
+#include <cstring>
 #include <mutex>
 
 namespace w4a16 {
@@ -96,22 +98,27 @@ struct Act<true> {
 // COLS columns in groups of W = min(COLS, 4) adjacent columns, one group per
 // 32*W columns, so every lane-wise shared-memory read of a warp covers
 // contiguous bytes (no bank conflicts).
+__host__ __device__ constexpr int round128(int v) { return (v + 127) & ~127; }
+
 template <int COLS, int MT>
 struct Stage {
     static constexpr int CB = 32 * COLS;
     static constexpr int W = COLS < 4 ? COLS : 4;         // columns per group
     static constexpr int G = COLS / W;                    // groups per lane
-    static constexpr int kQ = 0;                          // [4][CB] uint32
-    static constexpr int kS = kQ + kRowsPerChunk * CB * 4;   // [CB] 16-bit scales
-    static constexpr int kZ = kS + CB * 2;                // [CB / 8] uint32
-    static constexpr int kX = kZ + CB / 2;                // [MT][32] 16-bit x
-    static constexpr int kBytes = kX + MT * kChunk * 2;
-    static_assert(kS % 16 == 0 && kZ % 16 == 0 && kX % 16 == 0 && kBytes % 16 == 0, "16-byte aligned blocks");
+    // every block is a tensor-copy destination: 128-byte aligned
+    static constexpr int kQ = 0;                                          // [4][CB] uint32
+    static constexpr int kS = kQ + round128(kRowsPerChunk * CB * 4);      // [CB] 16-bit scales
+    static constexpr int kZ = kS + round128(CB * 2);                      // [CB / 8] uint32
+    static constexpr int kX = kZ + round128(CB / 2);                      // [MT][32] 16-bit x
+    static constexpr int kBytes = kX + round128(MT * kChunk * 2);
+    static_assert(kS % 128 == 0 && kZ % 128 == 0 && kX % 128 == 0 && kBytes % 128 == 0,
+                  "tensor-copy destinations must be 128-byte aligned");
     __device__ static int col(int lane, int gi, int u) { return gi * 32 * W + lane * W + u; }
 };
 
 __host__ __device__ constexpr int stage_bytes(int cols, int mt) {
-    return 32 * cols * (kRowsPerChunk * 4 + 2) + 32 * cols / 2 + mt * kChunk * 2;
+    return round128(kRowsPerChunk * 32 * cols * 4) + round128(32 * cols * 2) + round128(32 * cols / 2) +
+           round128(mt * kChunk * 2);
 }
 
 template <int BYTES>
@@ -127,12 +134,6 @@ __device__ __forceinline__ void lds(uint32_t addr, uint32_t (&v)[(BYTES + 3) / 4
         asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h) : "r"(addr));
         v[0] = h;
     }
-}
-
-__device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-                 "l"(src), "r"(bytes), "r"(bar)
-                 : "memory");
 }
 
 // Lane 0 waits, bounded (about two seconds), sleeping in try_wait; then every
@@ -158,17 +159,25 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int lan
 }
 
 struct GemvArgs {
-    const uint16_t* x;
-    const uint32_t* qw;
-    const uint16_t* sc;
+    CUtensorMap tq;       // qweight int32 [K/8, N], box [4 rows, CB]
+    CUtensorMap ts;       // scales 16-bit [K/g, N], box [1, CB]
+    CUtensorMap tz;       // qzeros int32 [K/g, N/8], box [1, CB/8] (used when N % 32 == 0)
+    CUtensorMap tx;       // x 16-bit [M, K], box [MT rows, 32]
     const uint32_t* qz;
     uint16_t* y;
     uint32_t* tickets;    // [n_cb], zero between calls
     float* partials;      // [grid][2][M * CB], at most kMaxLive floats per slot
-    int M, N, K, g;
+    const uint16_t* x;
+    int M, N, K, g_shift;
     int chunks;
     long long items;      // n_cb * chunks
 };
+
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred = 0;
+    asm volatile("{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}" : "=r"(pred));
+    return pred != 0;
+}
 
 // Byte offsets inside dynamic shared memory: warp partials | chunk sums of x | barriers | rings.
 __host__ __device__ constexpr uint32_t xsum_offset(int live_per_warp) { return kWarps * live_per_warp * 4; }
@@ -186,7 +195,7 @@ __device__ __forceinline__ int owner_cta(long long i, long long T, int G) {
 __device__ __forceinline__ long long range_start(int b, long long T, int G) { return (long long)b * T / G; }
 
 template <bool kBf16, int MT, int COLS, bool kSym, bool kFact, bool kZBulk>
-__global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvArgs a) {
+__global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant__ GemvArgs a) {
     using A = Act<kBf16>;
     using St = Stage<COLS, MT>;
     constexpr int CB = St::CB;
@@ -196,8 +205,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ int s_last;
 
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int M = a.M, N = a.N, K = a.K, g = a.g, chunks = a.chunks;
+    const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x >> 5), 0);   // warp-uniform
+    const int lane = threadIdx.x & 31;
+    const int M = a.M, N = a.N, K = a.K, g_shift = a.g_shift, chunks = a.chunks;
     const long long T = a.items;
     const int Gd = gridDim.x, b = blockIdx.x;
     const long long i_begin = range_start(b, T, Gd), i_end = range_start(b + 1, T, Gd);
@@ -205,7 +215,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvArgs a) {
     float* red = reinterpret_cast<float*>(smem);                                   // [kWarps][E]
     float2* xsum = reinterpret_cast<float2*>(smem + xsum_offset(E));               // [M][chunks]
     const uint32_t bars = smem_u32(smem) + bar_offset(E, xs_entries) + warp * kStages * 8;
-    const uint32_t ring = smem_u32(smem) + ring_offset(E, xs_entries) + warp * kStages * St::kBytes;
+    // rings start on a 128-byte boundary of the shared window (128 bytes of slack are reserved)
+    const uint32_t ring = ((smem_u32(smem) + ring_offset(E, xs_entries) + 127u) & ~127u) + warp * kStages * St::kBytes;
 
     if (lane == 0) {
         for (int st = 0; st < kStages; ++st) mbar_init(bars + 8 * st, 1);
@@ -249,22 +260,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvArgs a) {
 #pragma unroll
             for (int j = 0; j < COLS; ++j) yacc[m][j] = 0.f;
 
-        // lane 0: bring chunk c of this column block into stage st
+        // one lane: bring chunk c of this column block into stage st (tensor TMA, 4 copies)
         auto issue = [&](int st, int c) {
             const uint32_t base = ring + st * St::kBytes, bar = bars + 8 * st;
-            const int t = (c * kChunk) / g;
-            const uint32_t bytes = ncols * (kRowsPerChunk * 4 + 2) + (kZBulk ? ncols / 2 : 0) + M * kChunk * 2;
-            mbar_arrive_expect_tx(bar, bytes);
-            const uint32_t* q = a.qw + static_cast<size_t>(c) * kRowsPerChunk * N + static_cast<size_t>(cb) * CB;
-#pragma unroll
-            for (int i = 0; i < kRowsPerChunk; ++i)
-                bulk_copy(base + St::kQ + i * CB * 4, q + static_cast<size_t>(i) * N, ncols * 4, bar);
-            bulk_copy(base + St::kS, a.sc + static_cast<size_t>(t) * N + static_cast<size_t>(cb) * CB, ncols * 2, bar);
-            if constexpr (kZBulk)
-                bulk_copy(base + St::kZ, a.qz + static_cast<size_t>(t) * (N >> 3) + static_cast<size_t>(cb) * (CB / 8),
-                          ncols / 2, bar);
-            for (int m = 0; m < M; ++m)
-                bulk_copy(base + St::kX + m * kChunk * 2, a.x + static_cast<size_t>(m) * K + c * kChunk, kChunk * 2, bar);
+            const int t = (c * kChunk) >> g_shift;
+            constexpr uint32_t kBytes = kRowsPerChunk * CB * 4 + CB * 2 + (kZBulk ? CB / 2 : 0) + MT * kChunk * 2;
+            mbar_arrive_expect_tx(bar, kBytes);
+            tma_load_2d(base + St::kQ, &a.tq, cb * CB, c * kRowsPerChunk, bar);
+            tma_load_2d(base + St::kS, &a.ts, cb * CB, t, bar);
+            if constexpr (kZBulk) tma_load_2d(base + St::kZ, &a.tz, cb * (CB / 8), t, bar);
+            tma_load_2d(base + St::kX, &a.tx, c * kChunk, 0, bar);
         };
 
         auto compute = [&](int st, int c) {
@@ -281,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvArgs a) {
                         lds<4>(base + St::kZ + (c0l >> 3) * 4, v);
                         zw[gi] = v[0];
                     } else {
-                        const int t = (c * kChunk) / g;
+                        const int t = (c * kChunk) >> g_shift;
                         const int n = cb * CB + c0l;
                         zw[gi] = n < N ? __ldg(a.qz + static_cast<size_t>(t) * (N >> 3) + (n >> 3)) : 0u;
                     }
@@ -298,11 +303,25 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvArgs a) {
                 return A::to_float(static_cast<uint16_t>(sw[gi][u / 2] >> (16 * (u & 1))));
             };
 
+            // kFact: start each accumulator at -((magic + z) * sum x), so that after the
+            // chunk it holds sum (q - z) x; otherwise at 0 (z is subtracted per nibble)
             float acc[MT][COLS], acc2[kTwoFamilies ? MT : 1][kTwoFamilies ? COLS : 1];
+            if constexpr (kFact) {
+                float2 os[MT];
 #pragma unroll
-            for (int m = 0; m < MT; ++m)
+                for (int m = 0; m < MT; ++m) os[m] = (m < M) ? xsum[m * chunks + c] : make_float2(0.f, 0.f);
 #pragma unroll
-                for (int j = 0; j < COLS; ++j) acc[m][j] = 0.f;
+                for (int j = 0; j < COLS; ++j) {
+                    const float zf = static_cast<float>(zval(j));
+#pragma unroll
+                    for (int m = 0; m < MT; ++m) acc[m][j] = -fmaf(zf, os[m].y, os[m].x);
+                }
+            } else {
+#pragma unroll
+                for (int m = 0; m < MT; ++m)
+#pragma unroll
+                    for (int j = 0; j < COLS; ++j) acc[m][j] = 0.f;
+            }
             if constexpr (kTwoFamilies) {
 #pragma unroll
                 for (int m = 0; m < MT; ++m)
@@ -379,29 +398,23 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvArgs a) {
                     }
                 }
             }
-            // scale (and, for kFact, zero-point) once per chunk, in FP32
+            // scale once per chunk, in FP32
 #pragma unroll
             for (int j = 0; j < COLS; ++j) {
                 const float s = sval(j);
-                if constexpr (kFact) {
-                    const float zf = static_cast<float>(zval(j));
 #pragma unroll
-                    for (int m = 0; m < MT; ++m) {
-                        const float2 os = (m < M) ? xsum[m * chunks + c] : make_float2(0.f, 0.f);
-                        float t = acc[m][j];
-                        if constexpr (kTwoFamilies) t = fmaf(acc2[m][j], 0.0625f, t);
-                        yacc[m][j] = fmaf(s, t - fmaf(zf, os.y, os.x), yacc[m][j]);
-                    }
-                } else {
-#pragma unroll
-                    for (int m = 0; m < MT; ++m) yacc[m][j] = fmaf(s, acc[m][j], yacc[m][j]);
+                for (int m = 0; m < MT; ++m) {
+                    float t = acc[m][j];
+                    if constexpr (kTwoFamilies) t = fmaf(acc2[m][j], 0.0625f, t);
+                    yacc[m][j] = fmaf(s, t, yacc[m][j]);
                 }
             }
         };
 
         // this warp's chunks c0 + warp + kWarps * j, through its kStages-deep ring
-        if (lane == 0)
+        if (elect_one())
             for (int j = 0; j < kStages && j < nj; ++j) issue(j, c0 + warp + kWarps * j);
+        __syncwarp();
         for (int j = 0; j < nj; ++j) {
             const int st = j % kStages;
             if (!warp_wait(bars + 8 * st, (phase_bits >> st) & 1u, lane)) {
@@ -413,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvArgs a) {
             // every lane's reads of the stage precede the copy that refills it
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0 && j + kStages < nj) issue(st, c0 + warp + kWarps * (j + kStages));
+            if (j + kStages < nj && elect_one()) issue(st, c0 + warp + kWarps * (j + kStages));
         }
 
         // partial sums of the warps -> shared memory, reduced in warp order
@@ -540,7 +553,7 @@ GemvPlan plan_gemv(int M, int N, int K, int g, const DeviceProps& dp) {
     const size_t xsum_bytes = static_cast<size_t>(M) * chunks * sizeof(float2);
     p.fact = M <= kFactMaxM && xsum_bytes <= kXsumSmemLimit;
     const int live = p.mt * p.cb;
-    p.smem_bytes = ring_offset(live, p.fact ? M * chunks : 0) +
+    p.smem_bytes = ring_offset(live, p.fact ? M * chunks : 0) + 128 +
                    static_cast<size_t>(kWarps) * kStages * stage_bytes(p.cols, p.mt);
     // as many CTAs per SM as shared memory allows (at most 2), each with at least one chunk per warp
     const int per_sm = p.smem_bytes * 2 <= dp.smem_optin ? 2 : 1;
@@ -561,9 +574,23 @@ size_t gemv_workspace_bytes(const GemvPlan& p) { return p.ticket_bytes + p.parti
 cudaError_t launch_gemv(const void* x, const uint32_t* qw, const void* sc, const uint32_t* qz, void* y, int M,
                         int N, int K, int g, bool bf16, const GemvPlan& plan, void* workspace, cudaStream_t s) {
     GemvArgs a;
+    const CUtensorMapDataType act = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const uint32_t cb = static_cast<uint32_t>(plan.cb);
+    if (!encode_2d(&a.tq, CU_TENSOR_MAP_DATA_TYPE_INT32, qw, (uint64_t)N, (uint64_t)(K / 8), (uint64_t)N * 4, cb,
+                   kRowsPerChunk, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_2d(&a.ts, act, sc, (uint64_t)N, (uint64_t)(K / g), (uint64_t)N * 2, cb, 1,
+                   CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_2d(&a.tx, act, x, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, kChunk, plan.mt,
+                   CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    if (qz && N % 32 == 0) {
+        if (!encode_2d(&a.tz, CU_TENSOR_MAP_DATA_TYPE_INT32, qz, (uint64_t)(N / 8), (uint64_t)(K / g),
+                       (uint64_t)(N / 8) * 4, cb / 8, 1, CU_TENSOR_MAP_SWIZZLE_NONE))
+            return cudaErrorInvalidValue;
+    } else {
+        memset(&a.tz, 0, sizeof(a.tz));
+    }
     a.x = static_cast<const uint16_t*>(x);
-    a.qw = qw;
-    a.sc = static_cast<const uint16_t*>(sc);
     a.qz = qz;
     a.y = static_cast<uint16_t*>(y);
     a.partials = static_cast<float*>(workspace);
@@ -571,7 +598,7 @@ cudaError_t launch_gemv(const void* x, const uint32_t* qw, const void* sc, const
     a.M = M;
     a.N = N;
     a.K = K;
-    a.g = g;
+    a.g_shift = __builtin_ctz(static_cast<unsigned>(g));
     a.chunks = K / kChunk;
     a.items = plan.items;
     return bf16 ? launch_dtype<true>(a, plan, s) : launch_dtype<false>(a, plan, s);
