@@ -6,7 +6,8 @@
 //               (128-byte swizzle) and the packed weight tile [8 words x 128];
 //               the warp's lanes stage the step's scales and zero-point words
 //               with cp.async (zero-filled outside N and K). All of it lands
-//               in one stage of a 4-deep ring and completes one mbarrier.
+//               in one stage of a 5-deep ring and completes one mbarrier; the
+//               ring depth (bytes in flight per SM) is what bounds this kernel.
 //   warps 8-15  dequantise the packed tile ONCE into a [128 x 64] fp16/bf16
 //               operand tile in the canonical K-major 128-byte-swizzled layout
 //               the MMA reads: w = (q - z) * s, with (q - z) exact in 16-bit
@@ -48,8 +49,14 @@ namespace {
 
 constexpr int BM = 256, BN = 128, BK = 64;
 constexpr int UM = 128;                  // rows per tcgen05.mma: a tile is two M halves
-constexpr int kLoadStages = 4;           // x tile + packed weights + scales + zero-points
-constexpr int kBStages = 3;              // dequantised operand tiles
+#ifndef W4A16_GEMM_LOAD_STAGES
+#define W4A16_GEMM_LOAD_STAGES 5
+#endif
+#ifndef W4A16_GEMM_B_STAGES
+#define W4A16_GEMM_B_STAGES 2
+#endif
+constexpr int kLoadStages = W4A16_GEMM_LOAD_STAGES;   // x tile + packed weights + scales + zero-points
+constexpr int kBStages = W4A16_GEMM_B_STAGES;         // dequantised operand tiles
 constexpr int kThreads = 512;
 constexpr int kEpiWarp0 = 4;             // warps 4..7
 constexpr int kDeqWarp0 = 8;             // warps 8..15: two threads per column of the tile
@@ -99,17 +106,15 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
     }
 }
 
-// Lane 0 waits (bounded); then every lane of the warp observes the completed
-// phase itself. Returns the same verdict in every lane.
+// Lane 0 waits (bounded) and acquires the completed phase; the warp-wide
+// shuffle that broadcasts the verdict also orders the other lanes' later
+// accesses after lane 0's acquire. (Letting all 32 lanes poll one mbarrier
+// serialises their polls and costs hundreds of cycles per wait.)
 __device__ __forceinline__ bool warp_wait_bar(uint32_t bar, uint32_t parity, volatile int* abort, int lane) {
     int ok = 1;
     if (lane == 0) ok = wait_bar(bar, parity, abort) ? 1 : 0;
     ok = __shfl_sync(0xffffffffu, ok, 0);
-    if (ok && lane != 0) {
-        // the phase is already complete: this succeeds at once; bounded all the same
-        for (uint32_t i = 0; !mbar_try_wait(bar, parity) && i < (1u << 20); ++i) {
-        }
-    }
+    __syncwarp();
     return ok != 0;
 }
 

@@ -136,8 +136,10 @@ __device__ __forceinline__ void lds(uint32_t addr, uint32_t (&v)[(BYTES + 3) / 4
     }
 }
 
-// Lane 0 waits, bounded (about two seconds), sleeping in try_wait; then every
-// lane observes the completed phase itself.
+// Lane 0 waits, bounded (about two seconds), sleeping in try_wait, and
+// acquires the completed phase; the shuffle and warp barrier that follow order
+// the other lanes' reads of the stage after that acquire. (Letting all 32 lanes
+// poll one mbarrier serialises their polls and costs hundreds of cycles.)
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int lane) {
     int ok = 1;
     if (lane == 0 && !mbar_try_wait(bar, parity)) {
@@ -151,10 +153,7 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int lan
         }
     }
     ok = __shfl_sync(0xffffffffu, ok, 0);
-    if (ok && lane != 0) {
-        for (uint32_t i = 0; !mbar_try_wait(bar, parity) && i < (1u << 20); ++i) {
-        }
-    }
+    __syncwarp();
     return ok != 0;
 }
 
