@@ -55,8 +55,18 @@ namespace {
 #ifndef W4A16_GEMV_STAGES
 #define W4A16_GEMV_STAGES 2
 #endif
+// Chunks per warp whose weights are prefetched into L2 before the grid
+// dependency wait, and whether launches allow programmatic overlap with the
+// preceding kernel of the stream.
+#ifndef W4A16_GEMV_L2_PREFETCH
+#define W4A16_GEMV_L2_PREFETCH 2
+#endif
+#ifndef W4A16_GEMV_PDL
+#define W4A16_GEMV_PDL 1
+#endif
 constexpr int kWarps = W4A16_GEMV_WARPS;
 constexpr int kStages = W4A16_GEMV_STAGES;
+constexpr int kL2Prefetch = W4A16_GEMV_L2_PREFETCH;
 constexpr int kThreads = kWarps * 32;
 constexpr int kChunk = 32;            // rows of K per chunk
 constexpr int kRowsPerChunk = 4;      // packed word rows per chunk
@@ -217,12 +227,38 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     // rings start on a 128-byte boundary of the shared window (128 bytes of slack are reserved)
     const uint32_t ring = ((smem_u32(smem) + ring_offset(E, xs_entries) + 127u) & ~127u) + warp * kStages * St::kBytes;
 
+    // The next kernel of the stream may start its own prologue as this grid's
+    // CTAs exit. Before the dependency wait below this grid touches no caller
+    // data: it only initialises barriers and asks L2 for the weights of each
+    // warp's first chunks.
+    griddep_launch_dependents();
     if (lane == 0) {
         for (int st = 0; st < kStages; ++st) mbar_init(bars + 8 * st, 1);
         fence_mbar_init();
+        if (warp == 0) {
+            tma_prefetch_desc(&a.tq);
+            tma_prefetch_desc(&a.ts);
+            if constexpr (kZBulk) tma_prefetch_desc(&a.tz);
+            tma_prefetch_desc(&a.tx);
+        }
+        if (i_begin < i_end) {
+            const int cb = static_cast<int>(i_begin / chunks);
+            const int c0 = static_cast<int>(i_begin - static_cast<long long>(cb) * chunks);
+            const int c1 = static_cast<int>(std::min<long long>(chunks, c0 + (i_end - i_begin)));
+            for (int j = 0, c = c0 + warp; j < kL2Prefetch && c < c1; ++j, c += kWarps) {
+                const int t = (c * kChunk) >> g_shift;
+                tma_prefetch_l2_2d(&a.tq, cb * CB, c * kRowsPerChunk);
+                tma_prefetch_l2_2d(&a.ts, cb * CB, t);
+                if constexpr (kZBulk) tma_prefetch_l2_2d(&a.tz, cb * (CB / 8), t);
+            }
+        }
     }
-    if constexpr (kFact) {
-        // per (row, chunk): sum of x over the chunk, and the offset the magic bias adds
+    __syncthreads();
+    griddep_wait();
+
+    // per (row, chunk): sum of x over the chunk and the offset the magic bias
+    // adds; computed once, while the first copies are in flight
+    auto chunk_sums = [&]() {
         for (int p = threadIdx.x; p < M * chunks; p += kThreads) {
             const int m = p / chunks, c = p - m * chunks;
             const uint4* xp = reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(m) * K + c * kChunk);
@@ -240,17 +276,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
             const float off = kTwoFamilies ? (A::kMagicF * se + (A::kMagicF / 16.f) * so) : A::kMagicF * (se + so);
             xsum[p] = make_float2(off, se + so);
         }
-    }
-    __syncthreads();
+    };
 
     uint32_t phase_bits = 0;   // parity of the next completion of each stage's barrier
     bool ok = true;
+    bool sums_pending = kFact;
 
     for (long long it = i_begin; it < i_end;) {
         const int cb = static_cast<int>(it / chunks);
         const int c0 = static_cast<int>(it - static_cast<long long>(cb) * chunks);
         const int c1 = static_cast<int>(std::min<long long>(chunks, c0 + (i_end - it)));
-        const int ncols = std::min(CB, N - cb * CB);
         const int nj = ok ? (c1 - c0 - warp + kWarps - 1) / kWarps : 0;   // this warp's chunks
 
         float yacc[MT][COLS];
@@ -414,10 +449,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
         if (elect_one())
             for (int j = 0; j < kStages && j < nj; ++j) issue(j, c0 + warp + kWarps * j);
         __syncwarp();
+        if constexpr (kFact) {
+            if (sums_pending) {   // CTA-uniform: every thread runs the same segments
+                chunk_sums();
+                __syncthreads();
+                sums_pending = false;
+            }
+        }
+        int j_fail = -1;
         for (int j = 0; j < nj; ++j) {
             const int st = j % kStages;
             if (!warp_wait(bars + 8 * st, (phase_bits >> st) & 1u, lane)) {
                 ok = false;
+                j_fail = j;
                 break;
             }
             phase_bits ^= 1u << st;
@@ -426,6 +470,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
             fence_proxy_async_smem();
             __syncwarp();
             if (j + kStages < nj && elect_one()) issue(st, c0 + warp + kWarps * (j + kStages));
+        }
+        if (j_fail >= 0) {
+            // a wait ran out: wait (bounded) for this warp's copies still in
+            // flight, so none lands in shared memory after the CTA has exited
+            for (int j = j_fail; j < nj && j < j_fail + kStages; ++j) {
+                const int st = j % kStages;
+                if (!warp_wait(bars + 8 * st, (phase_bits >> st) & 1u, lane)) break;
+                phase_bits ^= 1u << st;
+            }
         }
 
         // partial sums of the warps -> shared memory, reduced in warp order
@@ -465,12 +518,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
             __syncthreads();
             if (s_last) {
                 __threadfence();
+                // Contributor b_lo covers the block's first chunks, so its segment
+                // starts at chunk 0 and it wrote slot 1; every later contributor
+                // starts inside the block and wrote slot 0 (no CTA has an empty
+                // range). Sums run in ascending CTA order, 8 loads in flight.
                 for (int e = threadIdx.x; e < EM; e += kThreads) {
-                    float sum = 0.f;
-                    for (int bb = b_lo; bb <= b_hi; ++bb) {
-                        const long long st = std::max(range_start(bb, T, Gd), first);
-                        const int sl = (st > first) ? 0 : 1;
-                        sum += __ldcg(a.partials + (static_cast<size_t>(bb) * 2 + sl) * EM + e);
+                    float sum = __ldcg(a.partials + (static_cast<size_t>(b_lo) * 2 + 1) * EM + e);
+                    for (int b0 = b_lo + 1; b0 <= b_hi; b0 += 8) {
+                        float v[8];
+#pragma unroll
+                        for (int u = 0; u < 8; ++u)
+                            v[u] = b0 + u <= b_hi ? __ldcg(a.partials + static_cast<size_t>(b0 + u) * 2 * EM + e) : 0.f;
+#pragma unroll
+                        for (int u = 0; u < 8; ++u)
+                            if (b0 + u <= b_hi) sum += v[u];
                     }
                     store_y(e, sum);
                 }
@@ -494,8 +555,17 @@ cudaError_t launch_one(const GemvArgs& a, const GemvPlan& p, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) configured[dev] = smem;
     }
-    kern<<<p.grid, kThreads, smem, s>>>(a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = W4A16_GEMV_PDL ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
 template <bool kBf16, int MT, int COLS, bool kFact>

@@ -64,6 +64,26 @@ __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
 
+// L2 prefetch of one tensor-map box. A hint only: it moves lines into L2 and
+// makes nothing visible to this thread, so it may run before the grid
+// dependency wait even on data a preceding kernel is still writing.
+__device__ __forceinline__ void tma_prefetch_l2_2d(const void* tmap, int32_t c0, int32_t c1) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(c0), "r"(c1)
+                 : "memory");
+}
+
+// Programmatic dependent launch. launch_dependents lets the next kernel of the
+// stream (if launched with programmatic serialization) start as SMs free up;
+// wait blocks until every prerequisite grid has completed and its memory
+// operations are visible. Both are no-ops for a kernel launched without the
+// attribute.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int32_t c0, int32_t c1,
                                             uint32_t bar) {
     asm volatile(
