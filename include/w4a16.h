@@ -127,10 +127,18 @@ size_t w4a16_workspace_bytes(w4a16_op op, int64_t M, int64_t N, int64_t K, int64
  * loads of the next 32-row chunk of K are in flight while the current one is
  * converted, which is the overlap whose absence the zero-point page blames for
  * its batch-4, g=128 regression (section "Known regression"). A persistent
- * grid of two CTAs per SM takes equal shares of (column block, K chunk) items,
- * so every SM streams the same bytes; a column block shared by several CTAs
- * is finished by the last of them to arrive, which sums the partial vectors
- * in ascending CTA order: the result is deterministic.
+ * grid (as many CTAs per SM as shared memory allows, at most two) takes equal
+ * shares of (column block, K chunk) items, so every SM streams the same
+ * bytes; a column block shared by several CTAs is finished by the last of
+ * them to arrive, which sums the partial vectors in ascending CTA order: the
+ * result is deterministic.
+ *
+ * The kernel is launched with programmatic stream serialization. Its prologue
+ * (barrier setup and an L2 prefetch of its first weight chunks, a cache hint
+ * that delivers no data to the kernel) may overlap the end of the preceding
+ * kernel on `stream`; every read of x, qweight, scales, qzeros and the
+ * workspace, and every write, happens after that kernel has completed and
+ * its memory operations are visible, exactly as for an ordinary launch.
  *
  * x        [M, K] dtype `dt`
  * qweight  int32 [K/8, N]
@@ -189,17 +197,19 @@ w4a16_status w4a16_gemv_noalloc(const void* x, const int32_t* qweight, const voi
 
 /*
  * w4a16_gemm -- prefill path, any M >= 1 (built for M in the hundreds or
- * more; small M works but wastes most of a 128-row tile).
+ * more; small M works but wastes most of a 256-row tile).
  *
- * Each CTA of a persistent grid owns 128 x 256 output tiles. Per 64-deep
- * K step, TMA brings the x tile and the packed weight tile into shared
- * memory, eight warps dequantise the weight tile ONCE into a shared bf16/fp16
- * operand tile that the whole tile's MMAs consume (the cooperative shared
- * tile of "ROCm KQuantGemmKWmmaQ4K/Q6K: redesign around a cooperative shared
- * tile", section "Confirmed mechanism"), and one thread issues tcgen05.mma
- * with the FP32 accumulator in tensor memory. M and N tails are handled by
- * TMA zero fill on loads and predicated stores. The dequantised weight is
- * (q - z) * s rounded once to the activation dtype.
+ * Clusters of two CTAs (one per SM) own 256 x 256 output tiles of a
+ * persistent grid. Per 64-deep K step each CTA brings its 128 rows of x and
+ * the packed weights of its 128 columns into shared memory with TMA, sixteen
+ * warps dequantise the weight tile ONCE into a shared bf16/fp16 operand tile
+ * that every MMA of the tile consumes (the cooperative shared tile of "ROCm
+ * KQuantGemmKWmmaQ4K/Q6K: redesign around a cooperative shared tile",
+ * section "Confirmed mechanism"), and one thread issues
+ * tcgen05.mma.cta_group::2 (M=256, N=256) over both CTAs' operands with the
+ * FP32 accumulator in tensor memory. M and N tails are handled by TMA zero
+ * fill on loads and predicated stores. The dequantised weight is (q - z) * s
+ * rounded once to the activation dtype.
  *
  * Arguments and errors as w4a16_gemv, except M >= 1 with no upper limit.
  * W4A16_ERR_TIMEOUT is never returned here; a pipeline wait that runs out

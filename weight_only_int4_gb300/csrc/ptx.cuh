@@ -199,6 +199,90 @@ __host__ __device__ constexpr uint32_t umma_idesc_f16(int M, int N, bool bf16) {
 }
 
 // ---------------------------------------------------------------------------
+// clusters and tcgen05 on a CTA pair (cta_group::2)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Every thread of every CTA of the cluster: arrive (release) and wait (acquire).
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Address in the shared window of cluster CTA `cta` of the object at local shared address `addr`.
+__device__ __forceinline__ uint32_t map_to_cta(uint32_t addr, uint32_t cta) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(cta));
+    return r;
+}
+
+// Arrive (release at cluster scope) on the mbarrier at local offset `bar` of cluster CTA `cta`.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar, uint32_t cta) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(map_to_cta(bar, cta))
+                 : "memory");
+}
+
+// Bounded-suspend try_wait with acquire at cluster scope: pairs with arrivals
+// made by the other CTA of the pair or by tensor-core commits multicast to it.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity, uint32_t suspend_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(suspend_ns)
+        : "memory");
+    return ok != 0;
+}
+
+// Store a 32-bit word to shared memory of cluster CTA `cta` at its local offset `addr`.
+__device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t cta, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(map_to_cta(addr, cta)), "r"(v) : "memory");
+}
+
+// One warp in EACH CTA of the pair executes these together: the pair's
+// allocation has the same base in both CTAs' tensor memory.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t slot, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot), "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// One thread of the pair's even CTA: D (+)= A * B^T over both CTAs. A's rows
+// [0, M/2) come from this CTA's shared memory at the descriptor's address and
+// rows [M/2, M) from the same address in the peer; B's N columns are split the
+// same way; each CTA's tensor memory receives its own M/2 rows of D.
+__device__ __forceinline__ void umma_f16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                              uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive once on the mbarrier at local offset `bar` of every CTA in `cta_mask`
+// when every tcgen05 operation issued so far by this thread completes.
+__device__ __forceinline__ void umma_commit_pair_mc(uint32_t bar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            bar),
+        "h"(cta_mask)
+        : "memory");
+}
+// As above, on this CTA's own mbarrier only.
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+// ---------------------------------------------------------------------------
 // bit tricks and mixed-precision FMA
 // ---------------------------------------------------------------------------
 // d = (a & b) | c  (one LOP3)
