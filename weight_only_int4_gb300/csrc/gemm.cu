@@ -29,7 +29,7 @@
 //               even CTA's operand barrier completes when its own dequant
 //               warps and one relay arrival for the odd CTA are in: both x
 //               blocks have landed and both operand tiles are written.
-//   warps 1-3   (odd CTA) relays: forward the odd CTA's tile completions to the
+//   warps 1-2   (odd CTA) relays: forward the odd CTA's tile completions to the
 //               even CTA with one cluster-scope release per K step, in turns.
 //   warp 1      (even CTA) one thread issues the MMAs into one of two
 //               256-column accumulators, which alternate so the epilogue of
@@ -76,7 +76,7 @@ constexpr int kEpiWarp0 = 4;             // warps 4..7
 constexpr int kDeqWarp0 = 8;             // warps 8..23: two groups taking alternate K steps
 constexpr int kDeqWarps = 8;             // per group: two threads per column of the CTA's tile
 constexpr int kDeqGroups = 2;
-constexpr int kRelayWarps = 3;           // odd CTA: warps 1..kRelayWarps forward operand-tile completions
+constexpr int kRelayWarps = 2;           // odd CTA: warps 1..kRelayWarps forward operand-tile completions
 constexpr uint32_t kABytes = CM * BK * 2;            // 16 KB
 constexpr uint32_t kWBytes = (BK / 8) * CN * 4;      //  4 KB
 constexpr uint32_t kSBytes = 2 * CN * 2;             // 512 B: scales of the two 32-row halves of a step
@@ -89,6 +89,18 @@ constexpr uint32_t kSuspendNs = 20000;
 constexpr unsigned long long kWaitLimitCycles = 4000000000ull;   // ~2 s at 2 GHz
 constexpr unsigned int kErrTimeout = 9u;
 static_assert(kTmemCols == 512, "tensor memory budget");
+// Parity waits are only sound if a waiter never reaches a barrier while a
+// phase it skipped is still open (it would take that phase's parity for its
+// own). Relays and dequant groups each own whole operand stages, so they
+// consume those barriers' phases in order. A dequant group skips the other
+// groups' load stages; when it waits for step j it has finished step j - G,
+// whose operand stage was freed by MMA j - G - B, and the in-order MMAs have
+// then consumed every load stage up to that step, which covers the skipped
+// step j - L whenever L >= G + B.
+static_assert(kBStages % kRelayWarps == 0, "each relay owns whole operand stages");
+static_assert(kBStages % kDeqGroups == 0, "each dequant group owns whole operand stages");
+static_assert(kLoadStages % kDeqGroups == 0 || kLoadStages >= kDeqGroups + kBStages,
+              "a dequant group may skip a load-stage phase only if it is already complete");
 
 struct __align__(8) Barriers {
     uint64_t lfull[kLoadStages];    // x + weights (TMA bytes) and scales/zero-points (cp.async) landed
@@ -126,6 +138,24 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ab
     for (;;) {
         if (kCluster ? mbar_try_wait_cluster(bar, parity, kSuspendNs) : mbar_try_wait_suspend(bar, parity, kSuspendNs))
             return true;
+        if (*ab.flag) return false;
+        if (clock64() - t0 > kWaitLimitCycles) {
+            *ab.flag = 1;
+            st_cluster_u32(ab.addr, ab.peer, 1u);
+            atomicOr(&g_device_error, 1u << kErrTimeout);
+            return false;
+        }
+    }
+}
+
+// As wait_bar, but polling without suspending: for the single threads whose
+// wake-up latency sits on the critical path (relays and the MMA issuer).
+template <bool kCluster = false>
+__device__ __forceinline__ bool spin_bar(uint32_t bar, uint32_t parity, const Abort& ab) {
+    const unsigned long long t0 = clock64();
+    for (;;) {
+        for (int i = 0; i < 64; ++i)
+            if (kCluster ? mbar_try_wait_cluster(bar, parity, 0) : mbar_try_wait(bar, parity)) return true;
         if (*ab.flag) return false;
         if (clock64() - t0 > kWaitLimitCycles) {
             *ab.flag = 1;
@@ -298,8 +328,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
         // A release at cluster scope holds the issuing thread for about a
         // microsecond, too long for the dequant warps to pay every step. They
         // arrive at CTA scope on bready; relay r forwards steps j = r (mod
-        // kRelayWarps) to the even CTA's bfull with one cluster-scope release,
-        // which also publishes the dequant warps' tile writes it acquired.
+        // kRelayWarps), i.e. operand stages r, r + kRelayWarps, ..., to the even
+        // CTA's bfull with one cluster-scope release, which also publishes the
+        // dequant warps' tile writes it acquired.
         if (lane == 0) {
             const int r = warp - 1;
             bool ok = true;
@@ -309,7 +340,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
                     if (j % kRelayWarps != r) continue;
                     const int bs = static_cast<int>(j % kBStages);
                     const uint32_t ph = static_cast<uint32_t>((j / kBStages) & 1);
-                    if (!wait_bar(smem_u32(&bars->bready[bs]), ph, ab)) { ok = false; break; }
+                    if (!spin_bar(smem_u32(&bars->bready[bs]), ph, ab)) { ok = false; break; }
                     mbar_arrive_cluster(smem_u32(&bars->bfull[bs]), 0);
                 }
             }
@@ -331,7 +362,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
                 for (int kt = 0; kt < kt_total; ++kt) {
                     // completes when both CTAs' x blocks landed and both operand tiles are written
                     // (the dequant warps wait for their CTA's x block before they arrive)
-                    if (!wait_bar<true>(smem_u32(&bars->bfull[bs]), bph, ab)) { ok = false; break; }
+                    if (!spin_bar<true>(smem_u32(&bars->bfull[bs]), bph, ab)) { ok = false; break; }
                     tc_fence_after();
                     const uint64_t adesc = sw128_kmajor_desc(ld_a(ls));
                     const uint64_t bdesc = sw128_kmajor_desc(op_b(bs));
