@@ -7,6 +7,7 @@ not L2). The headline workload is the gate_up-like decode GEMV
 GEMM 2048 x 43008 x 5376, g=32, bf16 ("prefill" object).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+    python bench.py --configs      # every named workload: median and min us per call
 
 Prints one JSON line on rank 0. `value` is the whole-job GB/s over all ranks
 (algorithmic bytes: packed weights + scales + packed zero-points + x + y).
@@ -188,6 +189,64 @@ def time_graph(layer, steps, warmup, torch, barrier):
     torch.cuda.synchronize()
     barrier()
     return t0.elapsed_time(t1) / 1e3   # seconds
+
+
+def time_graph_samples(layer, steps, warmup, torch):
+    """Per-replay device times (seconds) of a CUDA graph of one step."""
+    stream = torch.cuda.Stream()
+    for _ in range(max(1, warmup)):
+        layer.step()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        layer.step()
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        for e0, e1 in ev:
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+    torch.cuda.synchronize()
+    return [e0.elapsed_time(e1) / 1e3 for e0, e1 in ev]
+
+
+def run_configs(args):
+    """Every named workload on one GPU: median and min time per call over
+    `steps` replays of a graph of L calls on distinct weight copies (L chosen so
+    one replay streams >= 4x L2), GB/s of algorithmic bytes, TFLOP/s, and the
+    fractions of the measured peaks."""
+    import torch
+
+    import weight_only_int4_gb300 as w4
+    w4.load_library()
+    torch.cuda.set_device(0)
+    l2 = getattr(torch.cuda.get_device_properties(0), "L2_cache_size", 128 << 20)
+    peaks, peak_src = load_peaks()
+    rows = []
+    clocks = ClockSampler(0)
+    clocks.start()
+    for name, wl in WORKLOADS.items():
+        per = layer_bytes(wl.M, wl.N, wl.K, wl.g, wl.symmetric, wl.act).total
+        L = copies_for(per, l2) if wl.kernel == "gemv" else 2
+        layer = Layer(name, L, torch, w4)
+        steps = max(5, args.steps if wl.kernel == "gemv" else args.steps // 10)
+        t = [x / L for x in time_graph_samples(layer, steps, max(3, args.warmup), torch)]
+        med, mn = statistics.median(t), min(t)
+        rows.append({"workload": name, "kernel": wl.kernel, "calls_per_replay": L, "replays": steps,
+                     "us_median": round(med * 1e6, 3), "us_min": round(mn * 1e6, 3),
+                     "GBs": round(per / med / 1e9, 1), "TFLOPs": round(layer.flops / med / 1e12, 2),
+                     "frac_hbm": round(per / med / 1e9 / peaks["hbm_gbs"], 4),
+                     "frac_bf16": round(layer.flops / med / 1e12 / peaks["bf16_tflops"], 4)})
+        del layer
+        torch.cuda.empty_cache()
+    clk = clocks.stop()
+    if w4.device_status() != w4.OK:
+        raise RuntimeError("device-side error status after the timed region")
+    return {"configs": rows, "peaks": peaks, "peak_source": peak_src, "clocks": clk,
+            "timing": "per-replay CUDA events around a CUDA graph of L calls; per call = replay / L"}
 
 
 def time_e2e(layer, steps, warmup, torch):
@@ -382,6 +441,24 @@ def run_reference(args):
     }
 
 
+def dist_helpers(device):
+    """Barrier and max-over-ranks of a float for the replicas (the process group
+    is already initialised): every rank's timed region is bracketed by the
+    barrier, and the job's time is the slowest rank's."""
+    import torch
+    import torch.distributed as dist
+
+    def barrier():
+        dist.barrier()
+
+    def allmax(v):
+        t = torch.tensor([v], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    return barrier, allmax
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -392,6 +469,7 @@ def main():
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--configs", action="store_true", help="time every named workload (one GPU) and exit")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -403,6 +481,10 @@ def main():
         if rank == 0:
             print(json.dumps(run_reference(args)), flush=True)
         return
+    if args.configs:
+        if rank == 0:
+            print(json.dumps(run_configs(args)), flush=True)
+        return
 
     barrier = lambda: None  # noqa: E731
     allmax = lambda v: v    # noqa: E731
@@ -411,14 +493,7 @@ def main():
         import torch.distributed as dist
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
         dist.init_process_group("nccl")
-
-        def barrier():
-            dist.barrier()
-
-        def allmax(v):
-            t = torch.tensor([v], dtype=torch.float64, device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            return float(t.item())
+        barrier, allmax = dist_helpers("cuda")
 
     line = run_ours(args, rank, world, barrier, allmax)
     if rank == 0:
