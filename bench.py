@@ -226,6 +226,7 @@ def run_configs(args):
     l2 = getattr(torch.cuda.get_device_properties(0), "L2_cache_size", 128 << 20)
     peaks, peak_src = load_peaks()
     rows = []
+    copy_gbs = box_copy_gbs(torch)
     clocks = ClockSampler(0)
     clocks.start()
     for name, wl in WORKLOADS.items():
@@ -246,6 +247,7 @@ def run_configs(args):
     if w4.device_status() != w4.OK:
         raise RuntimeError("device-side error status after the timed region")
     return {"configs": rows, "peaks": peaks, "peak_source": peak_src, "clocks": clk,
+            "this_gpu_copy_gbs": copy_gbs,
             "timing": "per-replay CUDA events around a CUDA graph of L calls; per call = replay / L"}
 
 
@@ -275,6 +277,27 @@ def time_e2e(layer, steps, warmup, torch):
     return dt, h2d, d2h
 
 
+def box_copy_gbs(torch, nbytes=1 << 30, reps=5):
+    """Device-to-device copy bandwidth of this GPU (bytes read + written per
+    second): context for the roofline, which is taken against the measured
+    peak. GB300s of one pool differ by several per cent here."""
+    src = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    dst = torch.empty_like(src)
+    for _ in range(2):
+        dst.copy_(src)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(reps):
+        dst.copy_(src)
+    e1.record()
+    torch.cuda.synchronize()
+    gbs = 2 * nbytes * reps / (e0.elapsed_time(e1) / 1e3) / 1e9
+    del src, dst
+    torch.cuda.empty_cache()
+    return round(gbs, 1)
+
+
 def copies_for(bytes_per_layer, l2_bytes):
     """Enough weight copies that one step moves >= 1 GB and >= 4x L2."""
     target = max(1e9, 4 * l2_bytes)
@@ -300,6 +323,7 @@ def run_ours(args, rank, world, barrier, allmax):
     wl = WORKLOADS[args.workload]
     per_layer = layer_bytes(wl.M, wl.N, wl.K, wl.g, wl.symmetric, wl.act).total
     L = copies_for(per_layer, l2)
+    copy_gbs = box_copy_gbs(torch)
     layer = Layer(args.workload, L, torch, w4)
 
     clocks = ClockSampler(local)
@@ -344,7 +368,9 @@ def run_ours(args, rank, world, barrier, allmax):
                      "peak_source": peak_src,
                      "traffic": load_traffic("gemv", args.workload),
                      "kernel": "gemv_kernel", "algorithmic_bytes_per_launch": bytes_per_launch,
-                     "us_per_launch": round(launch_s * 1e6, 3)},
+                     "us_per_launch": round(launch_s * 1e6, 3),
+                     "context": {"this_gpu_copy_gbs": copy_gbs,
+                                 "frac_of_this_gpu_copy": round(achieved / copy_gbs, 4)}},
         "clocks": clk,
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
