@@ -231,6 +231,19 @@ w4a16_status w4a16_gemm(const void* x, const int32_t* qweight, const void* scale
  */
 w4a16_status w4a16_device_status(w4a16_stream stream);
 
+/*
+ * w4a16_selftest_wait_timeout -- exercise the device-side failure path. (No
+ * counterpart on the pages this library follows.)
+ *
+ * Launches, asynchronously on `stream`, one warp that waits on an mbarrier
+ * nothing will complete, with the same bounded wait the GEMV uses. After about
+ * two seconds the wait gives up, records W4A16_ERR_TIMEOUT in the device error
+ * word and the kernel exits normally, so the CUDA context stays usable; a
+ * following w4a16_device_status(stream) returns W4A16_ERR_TIMEOUT (and clears
+ * the word). Touches no caller memory. Errors: DEVICE, CUDA (launch failed).
+ */
+w4a16_status w4a16_selftest_wait_timeout(w4a16_stream stream);
+
 /* Human-readable name of a status code (static storage, never NULL). */
 const char* w4a16_status_string(w4a16_status status);
 

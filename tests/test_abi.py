@@ -113,6 +113,7 @@ def test_valid_arguments_stop_at_the_device_gate(lib):
     assert _gemm(lib) == w4.ERR_DEVICE
     assert lib.w4a16_pack(P, P, 8, 8, 0, None) == w4.ERR_DEVICE
     assert lib.w4a16_device_status(None) == w4.ERR_DEVICE
+    assert lib.w4a16_selftest_wait_timeout(None) == w4.ERR_DEVICE
     assert lib.w4a16_workspace_bytes(w4.OP_GEMV, 1, 64, 128, 32) == 0
 
 

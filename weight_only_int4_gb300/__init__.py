@@ -51,6 +51,7 @@ SIGNATURES = {
     "w4a16_gemm": (_INT, _LAYER_ARGS),
     "w4a16_gemv_noalloc": (_INT, [_VP, _VP, _VP, _VP, _VP, _I64, _I64, _I64, _I64, _INT, _VP]),
     "w4a16_device_status": (_INT, [_VP]),
+    "w4a16_selftest_wait_timeout": (_INT, [_VP]),
     "w4a16_status_string": (ctypes.c_char_p, [_INT]),
     "w4a16_abi_version": (_INT, []),
 }
@@ -239,3 +240,10 @@ def gemm(x, qweight, scales, qzeros: Optional[object], group_size: int, out=None
 def device_status(stream=None) -> int:
     """Synchronise the stream, return and clear the device-side error status."""
     return int(load_library().w4a16_device_status(_stream_ptr(stream)))
+
+
+def selftest_wait_timeout(stream=None) -> None:
+    """Launch the bounded-wait self-test (one warp waits on a barrier nothing
+    completes; it gives up after about two seconds and records
+    W4A16_ERR_TIMEOUT, which `device_status` then returns)."""
+    _check("w4a16_selftest_wait_timeout", load_library().w4a16_selftest_wait_timeout(_stream_ptr(stream)))

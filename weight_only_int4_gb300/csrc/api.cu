@@ -191,4 +191,12 @@ w4a16_status w4a16_device_status(w4a16_stream stream) {
     return (v | u) ? W4A16_ERR_TIMEOUT : W4A16_OK;
 }
 
+w4a16_status w4a16_selftest_wait_timeout(w4a16_stream stream) {
+    DeviceProps dp;
+    w4a16_status st = device_gate(&dp);
+    if (st != W4A16_OK) return st;
+    return w4a16::launch_wait_selftest(reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? W4A16_OK
+                                                                                          : W4A16_ERR_CUDA;
+}
+
 }  // extern "C"

@@ -700,6 +700,31 @@ cudaError_t gemv_noalloc_scratch(int device, void** ptr) {
     return cudaSuccess;
 }
 
+// ---------------------------------------------------------------------------
+// Self-test of the bounded wait
+// ---------------------------------------------------------------------------
+namespace {
+// One warp waits, with the kernels' own bounded wait, on an mbarrier that
+// nothing will complete: after about two seconds the wait gives up, records
+// W4A16_ERR_TIMEOUT in the GEMV error word and the kernel returns normally.
+__global__ void wait_selftest_kernel() {
+    __shared__ __align__(8) uint64_t bar;
+    const uint32_t b = smem_u32(&bar);
+    const int lane = threadIdx.x & 31;
+    if (lane == 0) {
+        mbar_init(b, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    (void)warp_wait(b, 0, lane);
+}
+}  // namespace
+
+cudaError_t launch_wait_selftest(cudaStream_t s) {
+    wait_selftest_kernel<<<1, 32, 0, s>>>();
+    return cudaGetLastError();
+}
+
 cudaError_t read_and_clear_gemv_error(uint32_t* out) {
     uint32_t v = 0;
     cudaError_t e = cudaMemcpyFromSymbol(&v, g_gemv_error, sizeof(v));
