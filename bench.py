@@ -33,7 +33,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from w4a16_inputs import WORKLOADS  # noqa: E402
-from weight_only_int4_gb300.accounting import layer_bytes, layer_flops  # noqa: E402
+from weight_only_int4_gb300.accounting import dequant_bytes, layer_bytes, layer_flops  # noqa: E402
 
 METRIC = "W4A16 GEMM GB/s (% of HBM peak) at M=1-4; TFLOP/s (% bf16 peak) at M=2048"
 DECODE = "gemv_1x43008x5376_g32_f16_asym"
@@ -151,8 +151,14 @@ class Layer:
         qz = None if case.z is None else w4.pack(torch.from_numpy(case.z).cuda(), dim=1)
         self.weights = [(qw, s, qz)] + [(qw.clone(), s.clone(), None if qz is None else qz.clone())
                                         for _ in range(copies - 1)]
-        self.y = [torch.empty((wl.M, wl.N), dtype=self.x.dtype, device="cuda") for _ in range(copies)]
         self.fn = getattr(w4, wl.kernel)
+        if wl.kernel == "dequant":
+            self.y = [torch.empty((wl.K, wl.N), dtype=self.x.dtype, device="cuda") for _ in range(copies)]
+            self.ws = None
+            self.bytes = dequant_bytes(wl.N, wl.K, wl.g, wl.symmetric, wl.act)
+            self.flops = 0
+            return
+        self.y = [torch.empty((wl.M, wl.N), dtype=self.x.dtype, device="cuda") for _ in range(copies)]
         op = w4.OP_GEMV if wl.kernel == "gemv" else w4.OP_GEMM
         nws = w4.workspace_bytes(op, wl.M, wl.N, wl.K, wl.g)
         self.ws = w4.new_workspace(nws) if nws else None
@@ -160,6 +166,10 @@ class Layer:
         self.flops = layer_flops(wl.M, wl.N, wl.K)
 
     def step(self, x=None):
+        if self.wl.kernel == "dequant":
+            for (qw, s, qz), y in zip(self.weights, self.y):
+                self.fn(qw, s, qz, self.wl.g, out=y)
+            return
         x = self.x if x is None else x
         for (qw, s, qz), y in zip(self.weights, self.y):
             self.fn(x, qw, s, qz, self.wl.g, out=y, workspace=self.ws)
@@ -230,10 +240,11 @@ def run_configs(args):
     clocks = ClockSampler(0)
     clocks.start()
     for name, wl in WORKLOADS.items():
-        per = layer_bytes(wl.M, wl.N, wl.K, wl.g, wl.symmetric, wl.act).total
-        L = copies_for(per, l2) if wl.kernel == "gemv" else 2
+        per = (dequant_bytes(wl.N, wl.K, wl.g, wl.symmetric, wl.act) if wl.kernel == "dequant" else
+               layer_bytes(wl.M, wl.N, wl.K, wl.g, wl.symmetric, wl.act)).total
+        L = copies_for(per, l2) if wl.kernel != "gemm" else 2
         layer = Layer(name, L, torch, w4)
-        steps = max(5, args.steps if wl.kernel == "gemv" else args.steps // 10)
+        steps = max(5, args.steps if wl.kernel != "gemm" else args.steps // 10)
         t = [x / L for x in time_graph_samples(layer, steps, max(3, args.warmup), torch)]
         med, mn = statistics.median(t), min(t)
         rows.append({"workload": name, "kernel": wl.kernel, "calls_per_replay": L, "replays": steps,

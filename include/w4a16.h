@@ -221,6 +221,25 @@ w4a16_status w4a16_gemm(const void* x, const int32_t* qweight, const void* scale
                         w4a16_stream stream);
 
 /*
+ * w4a16_dequant -- dense dequantised copy of the packed weights:
+ *
+ *     w[k, n] = RN((q[k, n] - z[k / g, n]) * s[k / g, n])
+ *
+ * in dtype `dt`, row-major [K, N]: the dense dequantised weight copy that
+ * "Keep W4A16 zero-points packed at 4 bits instead of expanding to 2 bytes"
+ * (section "Change") builds at load time beside the skinny GEMM. (q - z) is exact in 16-bit
+ * arithmetic and the product is rounded once, so the result is bit-exact.
+ *
+ * qweight  int32 [K/8, N]; scales [K/g, N] dtype `dt`; qzeros int32
+ *          [K/g, N/8] or NULL (symmetric, z = 8)
+ * w        [K, N] dtype `dt`, written (device memory owned by the caller)
+ * Errors: NULL, SHAPE (N % 8, K % g, non-positive), UNSUPPORTED (g), DTYPE,
+ * ALIGN, DEVICE, CUDA. Streams each operand once; bound by HBM bandwidth.
+ */
+w4a16_status w4a16_dequant(const int32_t* qweight, const void* scales, const int32_t* qzeros, void* w, int64_t N,
+                           int64_t K, int64_t g, w4a16_dtype dt, w4a16_stream stream);
+
+/*
  * w4a16_device_status -- synchronise `stream`, then read and clear the
  * device-side error word of the current device. Every wait on an mbarrier
  * inside the GEMM pipeline gives up after about two seconds; the kernel then

@@ -89,6 +89,19 @@ def test_gemv_needs_an_aligned_workspace(lib):
     assert _gemv(lib, ws=MIS) == w4.ERR_WORKSPACE
 
 
+def test_dequant_rejections(lib):
+    d = lambda **kw: lib.w4a16_dequant(kw.get("qw", P), kw.get("s", P), kw.get("z", P), kw.get("w", P),
+                                       kw.get("N", 64), kw.get("K", 128), kw.get("g", 32), kw.get("dt", w4.F16), None)
+    assert d(qw=None) == w4.ERR_NULL
+    assert d(w=None) == w4.ERR_NULL
+    assert d(dt=5) == w4.ERR_DTYPE
+    assert d(N=60) == w4.ERR_SHAPE
+    assert d(K=100) == w4.ERR_SHAPE
+    assert d(g=48, K=96) == w4.ERR_UNSUPPORTED
+    assert d(w=MIS) == w4.ERR_ALIGN
+    assert d(z=MIS) == w4.ERR_ALIGN
+
+
 def test_pack_rejections(lib):
     assert lib.w4a16_pack(None, P, 8, 8, 0, None) == w4.ERR_NULL
     assert lib.w4a16_pack(P, P, 12, 8, 0, None) == w4.ERR_SHAPE      # rows % 8 for dim 0
@@ -114,6 +127,7 @@ def test_valid_arguments_stop_at_the_device_gate(lib):
     assert lib.w4a16_pack(P, P, 8, 8, 0, None) == w4.ERR_DEVICE
     assert lib.w4a16_device_status(None) == w4.ERR_DEVICE
     assert lib.w4a16_selftest_wait_timeout(None) == w4.ERR_DEVICE
+    assert lib.w4a16_dequant(P, P, P, P, 64, 128, 32, w4.F16, None) == w4.ERR_DEVICE
     assert lib.w4a16_workspace_bytes(w4.OP_GEMV, 1, 64, 128, 32) == 0
 
 

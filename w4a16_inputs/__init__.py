@@ -111,7 +111,7 @@ class Workload:
     """A named problem shape. `kernel` is the entry point that serves it."""
 
     name: str
-    kernel: str  # "gemv" or "gemm"
+    kernel: str  # "gemv", "gemm" or "dequant"
     M: int
     N: int
     K: int
@@ -142,6 +142,15 @@ WORKLOADS = {w.name: w for w in [
       for (N, K) in ((16384, 5376), (5376, 21504)) for s in (True, False)],
     # prefill GEMM on the gate_up shape, g=32, bf16 in/out
     _w("gemm_2048x43008x5376_g32_bf16_asym", "gemm", 2048, 43008, 5376, 32, "bf16", False),
+    # the same prefill shape in fp16, and with g=128
+    _w("gemm_2048x43008x5376_g32_f16_asym", "gemm", 2048, 43008, 5376, 32, "f16", False),
+    _w("gemm_2048x43008x5376_g128_bf16_asym", "gemm", 2048, 43008, 5376, 128, "bf16", False),
+    # mid-M prefill chunks on the same weights
+    _w("gemm_64x43008x5376_g32_bf16_asym", "gemm", 64, 43008, 5376, 32, "bf16", False),
+    _w("gemm_256x43008x5376_g32_bf16_asym", "gemm", 256, 43008, 5376, 32, "bf16", False),
+    # dense dequantised copy of the gate_up weights (M is unused)
+    _w("dequant_43008x5376_g32_f16_asym", "dequant", 1, 43008, 5376, 32, "f16", False),
+    _w("dequant_43008x5376_g32_bf16_asym", "dequant", 1, 43008, 5376, 32, "bf16", False),
 ]}
 
 

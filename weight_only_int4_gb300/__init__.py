@@ -52,6 +52,7 @@ SIGNATURES = {
     "w4a16_gemv_noalloc": (_INT, [_VP, _VP, _VP, _VP, _VP, _I64, _I64, _I64, _I64, _INT, _VP]),
     "w4a16_device_status": (_INT, [_VP]),
     "w4a16_selftest_wait_timeout": (_INT, [_VP]),
+    "w4a16_dequant": (_INT, [_VP, _VP, _VP, _VP, _I64, _I64, _I64, _INT, _VP]),
     "w4a16_status_string": (ctypes.c_char_p, [_INT]),
     "w4a16_abi_version": (_INT, []),
 }
@@ -235,6 +236,38 @@ def gemm(x, qweight, scales, qzeros: Optional[object], group_size: int, out=None
          stream=None):
     """Prefill path (any M >= 1, tcgen05 tensor cores). Returns y [M, N] in x's dtype."""
     return _layer("w4a16_gemm", x, qweight, scales, qzeros, group_size, out, workspace, stream)
+
+
+def dequant(qweight, scales, qzeros: Optional[object], group_size: int, out=None, stream=None):
+    """Dense dequantised copy W[k, n] = RN((q - z) * s) in the scales' dtype, [K, N]."""
+    torch = _torch()
+    for name, t in (("qweight", qweight), ("scales", scales)):
+        _cuda_contig(name, t)
+    if qweight.dim() != 2 or scales.dim() != 2:
+        raise ValueError("qweight and scales must be 2-D")
+    if qweight.dtype != torch.int32:
+        raise TypeError(f"qweight must be torch.int32, got {qweight.dtype}")
+    dt = _act_code(scales.dtype)
+    K, N = qweight.shape[0] * 8, qweight.shape[1]
+    if K % group_size or scales.shape != (K // group_size, N):
+        raise ValueError(f"scales shape {tuple(scales.shape)} does not match (K/g, N)")
+    zp = 0
+    if qzeros is not None:
+        _cuda_contig("qzeros", qzeros)
+        if qzeros.dtype != torch.int32:
+            raise TypeError(f"qzeros must be packed torch.int32 [K/g, N/8]; got {qzeros.dtype} "
+                            "(zero-points in the activation dtype are rejected)")
+        if qzeros.shape != (K // group_size, N // 8):
+            raise ValueError(f"qzeros shape {tuple(qzeros.shape)} does not match (K/g, N/8)")
+        zp = qzeros.data_ptr()
+    if out is None:
+        out = torch.empty((K, N), dtype=scales.dtype, device=scales.device)
+    _cuda_contig("out", out)
+    if out.shape != (K, N) or out.dtype != scales.dtype:
+        raise ValueError(f"out must be {scales.dtype} [K, N] = [{K}, {N}]")
+    _check("w4a16_dequant", load_library().w4a16_dequant(qweight.data_ptr(), scales.data_ptr(), zp, out.data_ptr(),
+                                                         N, K, group_size, dt, _stream_ptr(stream)))
+    return out
 
 
 def device_status(stream=None) -> int:

@@ -45,6 +45,13 @@ def layer_bytes(M: int, N: int, K: int, g: int, symmetric: bool = False, act: st
     )
 
 
+def dequant_bytes(N: int, K: int, g: int, symmetric: bool = False, act: str = "f16") -> LayerBytes:
+    """The dense dequantised copy: reads the packed operands once, writes K x N
+    activation-dtype values (counted as y; no x)."""
+    b = layer_bytes(1, N, K, g, symmetric, act)
+    return LayerBytes(weights=b.weights, scales=b.scales, zeros=b.zeros, x=0, y=K * N * ACT_BYTES[act])
+
+
 def expanded_zero_bytes(N: int, K: int, g: int, act: str = "f16") -> int:
     """Bytes of zero-points stored one activation-dtype value per (group, column)."""
     return (K // g) * N * ACT_BYTES[act]

@@ -191,6 +191,23 @@ w4a16_status w4a16_device_status(w4a16_stream stream) {
     return (v | u) ? W4A16_ERR_TIMEOUT : W4A16_OK;
 }
 
+w4a16_status w4a16_dequant(const int32_t* qweight, const void* scales, const int32_t* qzeros, void* w, int64_t N,
+                           int64_t K, int64_t g, w4a16_dtype dt, w4a16_stream stream) {
+    if (!qweight || !scales || !w) return W4A16_ERR_NULL;
+    if (dt != W4A16_F16 && dt != W4A16_BF16) return W4A16_ERR_DTYPE;
+    if (N < 1 || K < 1 || g < 1 || N > kMaxDim || K > kMaxDim) return W4A16_ERR_SHAPE;
+    if (N % 8 != 0 || K % g != 0) return W4A16_ERR_SHAPE;
+    if (!supported_group(g)) return W4A16_ERR_UNSUPPORTED;
+    if (!aligned16(qweight) || !aligned16(scales) || !aligned16(w) || (qzeros && !aligned16(qzeros)))
+        return W4A16_ERR_ALIGN;
+    DeviceProps dp;
+    w4a16_status st = device_gate(&dp);
+    if (st != W4A16_OK) return st;
+    return from_cuda(w4a16::launch_dequant(reinterpret_cast<const uint32_t*>(qweight), scales,
+                                           reinterpret_cast<const uint32_t*>(qzeros), w, (int)N, (int)K, (int)g,
+                                           dt == W4A16_BF16, dp, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 w4a16_status w4a16_selftest_wait_timeout(w4a16_stream stream) {
     DeviceProps dp;
     w4a16_status st = device_gate(&dp);

@@ -1,0 +1,135 @@
+// Dense dequantised copy of the packed weights,
+//
+//     W[k, n] = RN((q[k, n] - z[k / g, n]) * s[k / g, n])   in the activation dtype, row-major [K, N],
+//
+// the dense dequantised weight copy that "Keep W4A16 zero-points packed at 4
+// bits instead of expanding to 2 bytes" (section "Change") builds at load time
+// beside the skinny GEMM. A pure streaming kernel: per element it reads 0.5 byte of
+// packed code (plus 2.5/g of scale and zero-point) and writes 2 bytes, so it
+// is bound by HBM bandwidth.
+//
+// A thread owns one packed word row w (rows 8w .. 8w+7 of K) of 8 adjacent
+// columns: two 16-byte loads of qweight, one of the 8 scales and one packed
+// zero-point word; consecutive threads take consecutive column groups, so
+// loads and the 16-byte stores of each output row are coalesced. Per row and
+// column pair: a byte permute puts nibble j of both columns' words into the
+// low bits of two 16-bit halves, an OR with the exponent of 1024 (fp16) or
+// 128 (bf16) turns them into magic + q, one packed subtract of magic + z gives
+// the exact (q - z), one packed multiply by s rounds once.
+#include "internal.h"
+#include "ptx.cuh"
+
+#include <algorithm>
+
+namespace w4a16 {
+namespace {
+
+template <bool kBf16>
+struct Dq;
+template <>
+struct Dq<false> {
+    static constexpr uint32_t kMagic = 0x64006400u;   // fp16 1024.0 in both halves
+    __device__ static uint32_t sub2(uint32_t a, uint32_t b) {
+        uint32_t d;
+        asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+        return d;
+    }
+    __device__ static uint32_t mul2(uint32_t a, uint32_t b) {
+        uint32_t d;
+        asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+        return d;
+    }
+};
+template <>
+struct Dq<true> {
+    static constexpr uint32_t kMagic = 0x43004300u;   // bf16 128.0 in both halves
+    __device__ static uint32_t sub2(uint32_t a, uint32_t b) {
+        uint32_t d;
+        asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+        return d;
+    }
+    __device__ static uint32_t mul2(uint32_t a, uint32_t b) {
+        uint32_t d;
+        asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+        return d;
+    }
+};
+
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+__device__ __forceinline__ void st_stream(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+constexpr int kThreads = 256;
+
+template <bool kBf16, bool kSym>
+__global__ void __launch_bounds__(kThreads) dequant_kernel(const uint32_t* __restrict__ qw,
+                                                          const uint16_t* __restrict__ sc,
+                                                          const uint32_t* __restrict__ qz, uint16_t* __restrict__ out,
+                                                          int N, long long items, int g_shift) {
+    using D = Dq<kBf16>;
+    const int ng = N >> 3;   // column groups of 8
+    for (long long i = blockIdx.x * static_cast<long long>(kThreads) + threadIdx.x; i < items;
+         i += static_cast<long long>(gridDim.x) * kThreads) {
+        const long long w = i / ng;
+        const int c = static_cast<int>(i - w * ng);
+        const int t = static_cast<int>((w * 8) >> g_shift);    // the 8 rows lie in one group (8 | g)
+        const uint4 q0 = ld_stream(qw + w * N + 8 * c);
+        const uint4 q1 = ld_stream(qw + w * N + 8 * c + 4);
+        const uint4 s8 = ld_stream(sc + static_cast<long long>(t) * N + 8 * c);
+        const uint32_t zw = kSym ? 0x88888888u : __ldg(qz + static_cast<long long>(t) * ng + c);
+        const uint32_t ss[4] = {s8.x, s8.y, s8.z, s8.w};
+        uint32_t zz[4];
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            // (magic + z of column 2p, magic + z of column 2p+1)
+            zz[p] = D::kMagic | ((zw >> (8 * p)) & 0xFu) | (((zw >> (8 * p + 4)) & 0xFu) << 16);
+        }
+        uint32_t wd[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+        uint16_t* orow = out + (w * 8) * static_cast<long long>(N) + 8 * c;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            uint32_t o[4];
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                // low 16 bits of each column's word -> the two halves; keep nibble j (now in bits 0-3)
+                const uint32_t h = and_or(prmt(wd[2 * p], wd[2 * p + 1], 0x5410u), 0x000F000Fu, D::kMagic);
+                o[p] = D::mul2(D::sub2(h, zz[p]), ss[p]);
+            }
+            st_stream(orow + static_cast<long long>(j) * N, o[0], o[1], o[2], o[3]);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) wd[u] >>= 4;
+        }
+    }
+}
+
+template <bool kBf16, bool kSym>
+cudaError_t launch_typed(const uint32_t* qw, const void* sc, const uint32_t* qz, void* out, int N, int K, int g,
+                         const DeviceProps& dp, cudaStream_t s) {
+    const long long items = static_cast<long long>(K / 8) * (N / 8);
+    const long long want = (items + kThreads - 1) / kThreads;
+    const int grid = static_cast<int>(std::min<long long>(want, static_cast<long long>(dp.sms) * 8));
+    dequant_kernel<kBf16, kSym><<<grid, kThreads, 0, s>>>(qw, static_cast<const uint16_t*>(sc), qz,
+                                                          static_cast<uint16_t*>(out), N, items,
+                                                          __builtin_ctz(static_cast<unsigned>(g)));
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_dequant(const uint32_t* qw, const void* sc, const uint32_t* qz, void* out, int N, int K, int g,
+                           bool bf16, const DeviceProps& dp, cudaStream_t s) {
+    if (bf16)
+        return qz ? launch_typed<true, false>(qw, sc, qz, out, N, K, g, dp, s)
+                  : launch_typed<true, true>(qw, sc, qz, out, N, K, g, dp, s);
+    return qz ? launch_typed<false, false>(qw, sc, qz, out, N, K, g, dp, s)
+              : launch_typed<false, true>(qw, sc, qz, out, N, K, g, dp, s);
+}
+
+}  // namespace w4a16

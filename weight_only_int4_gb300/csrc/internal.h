@@ -62,5 +62,7 @@ cudaError_t read_and_clear_device_error(uint32_t* out, cudaStream_t s);
 // Read and clear the device-side error word of the GEMV rings (no sync).
 cudaError_t read_and_clear_gemv_error(uint32_t* out);
 cudaError_t launch_wait_selftest(cudaStream_t s);
+cudaError_t launch_dequant(const uint32_t* qw, const void* sc, const uint32_t* qz, void* out, int N, int K, int g,
+                           bool bf16, const DeviceProps& dp, cudaStream_t s);
 
 }  // namespace w4a16
