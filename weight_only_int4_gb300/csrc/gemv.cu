@@ -280,6 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
 
     uint32_t phase_bits = 0;   // parity of the next completion of each stage's barrier
     bool ok = true;
+    int drain_lo = 0, drain_hi = 0;   // after a timeout: this warp's chunks whose copies may be in flight
     bool sums_pending = kFact;
 
     for (long long it = i_begin; it < i_end;) {
@@ -456,12 +457,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
                 sums_pending = false;
             }
         }
-        int j_fail = -1;
         for (int j = 0; j < nj; ++j) {
             const int st = j % kStages;
             if (!warp_wait(bars + 8 * st, (phase_bits >> st) & 1u, lane)) {
                 ok = false;
-                j_fail = j;
+                drain_lo = j;
+                drain_hi = std::min(nj, j + kStages);
                 break;
             }
             phase_bits ^= 1u << st;
@@ -471,16 +472,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
             __syncwarp();
             if (j + kStages < nj && elect_one()) issue(st, c0 + warp + kWarps * (j + kStages));
         }
-        if (j_fail >= 0) {
-            // a wait ran out: wait (bounded) for this warp's copies still in
-            // flight, so none lands in shared memory after the CTA has exited
-            for (int j = j_fail; j < nj && j < j_fail + kStages; ++j) {
-                const int st = j % kStages;
-                if (!warp_wait(bars + 8 * st, (phase_bits >> st) & 1u, lane)) break;
-                phase_bits ^= 1u << st;
-            }
-        }
-
         // partial sums of the warps -> shared memory, reduced in warp order
 #pragma unroll
         for (int m = 0; m < MT; ++m)
@@ -540,6 +531,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
         }
         __syncthreads();   // red[] is reused by the next segment
         it += c1 - c0;
+    }
+    // only after a timeout: wait (bounded) for this warp's copies still in
+    // flight, so none lands in shared memory after the CTA has exited
+    if (lane == 0) {
+        for (int j = drain_lo; j < drain_hi; ++j) {
+            const int st = j % kStages;
+            const uint32_t par = (phase_bits >> st) & 1u;
+            const unsigned long long t0 = clock64();
+            while (!mbar_try_wait(bars + 8 * st, par) && clock64() - t0 < kWaitLimitCycles) {
+            }
+            phase_bits ^= 1u << st;
+        }
     }
 }
 
