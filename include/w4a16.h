@@ -196,8 +196,12 @@ w4a16_status w4a16_gemv_noalloc(const void* x, const int32_t* qweight, const voi
                                 int64_t g, w4a16_dtype dt, w4a16_stream stream);
 
 /*
- * w4a16_gemm -- prefill path, any M >= 1 (built for M in the hundreds or
- * more; small M works but wastes most of a 256-row tile).
+ * w4a16_gemm -- prefill path, any M >= 1.
+ *
+ * M <= 128 runs an operand-swapped kernel: one CTA per 128 weight columns,
+ * the dequantised weight tile as the MMA's 128-row operand and x (padded to
+ * 32, 64 or 128 rows) as the other, so no MMA work is spent on 256-row tiles.
+ * Larger M runs the kernel described next.
  *
  * Clusters of two CTAs (one per SM) own 256 x 256 output tiles of a
  * persistent grid. Per 64-deep K step each CTA brings its 128 rows of x and

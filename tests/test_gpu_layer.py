@@ -72,6 +72,15 @@ def test_gemm_parity(act, g, sym, M):
         parity("gemm", M, N, K, g, act, sym, seed=M + N + K)
 
 
+@pytest.mark.parametrize("M", [32, 33, 64, 65, 127, 129])
+@pytest.mark.parametrize("act", ["bf16", "f16"])
+def test_gemm_row_buckets(M, act):
+    """Both sides of every padding step of the operand-swapped kernel (32, 64, 128
+    rows of x) and of its hand-over to the CTA-pair kernel above 128 rows."""
+    parity("gemm", M, 776, 384, 32, act, False, seed=M)
+    parity("gemm", M, 264, 256, 128, act, True, seed=M + 1)
+
+
 @pytest.mark.parametrize("g", [64, 256])
 def test_gemm_other_groups(g):
     parity("gemm", 200, 520, 2 * g * 3, g, "bf16", False, seed=g)

@@ -20,7 +20,7 @@ BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_DIR = os.path.join(PKG, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libw4a16.so")
 
-SOURCES = ["api.cu", "pack.cu", "gemv.cu", "gemm.cu", "dequant.cu"]
+SOURCES = ["api.cu", "pack.cu", "gemv.cu", "gemm.cu", "gemm_skinny.cu", "dequant.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", INCLUDE, "-I", CSRC]

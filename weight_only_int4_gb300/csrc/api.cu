@@ -175,6 +175,11 @@ w4a16_status w4a16_gemm(const void* x, const int32_t* qweight, const void* scale
     if (st != W4A16_OK) return st;
     DeviceProps dp;
     if ((st = device_gate(&dp)) != W4A16_OK) return st;
+    if (M <= w4a16::kSkinnyMaxM)
+        return from_cuda(w4a16::launch_gemm_skinny(x, reinterpret_cast<const uint32_t*>(qweight), scales,
+                                                   reinterpret_cast<const uint32_t*>(qzeros), y, (int)M, (int)N,
+                                                   (int)K, (int)g, dt == W4A16_BF16, dp,
+                                                   reinterpret_cast<cudaStream_t>(stream)));
     return from_cuda(w4a16::launch_gemm(x, reinterpret_cast<const uint32_t*>(qweight), scales,
                                         reinterpret_cast<const uint32_t*>(qzeros), y, (int)M, (int)N, (int)K, (int)g,
                                         dt == W4A16_BF16, dp, reinterpret_cast<cudaStream_t>(stream)));
@@ -184,11 +189,11 @@ w4a16_status w4a16_device_status(w4a16_stream stream) {
     DeviceProps dp;
     w4a16_status st = device_gate(&dp);
     if (st != W4A16_OK) return st;
-    uint32_t v = 0, u = 0;
+    uint32_t v = 0, u = 0, k = 0;
     if (w4a16::read_and_clear_device_error(&v, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess ||
-        w4a16::read_and_clear_gemv_error(&u) != cudaSuccess)
+        w4a16::read_and_clear_gemv_error(&u) != cudaSuccess || w4a16::read_and_clear_skinny_error(&k) != cudaSuccess)
         return W4A16_ERR_CUDA;
-    return (v | u) ? W4A16_ERR_TIMEOUT : W4A16_OK;
+    return (v | u | k) ? W4A16_ERR_TIMEOUT : W4A16_OK;
 }
 
 w4a16_status w4a16_dequant(const int32_t* qweight, const void* scales, const int32_t* qzeros, void* w, int64_t N,

@@ -1,0 +1,449 @@
+// GEMM of the W4A16 layer for a few rows of x (M <= 128) on the
+// 5th-generation tensor cores, with the operands swapped.
+//
+// For small M the weights dominate everything: the layer must stream and
+// dequantise K*N weights whatever M is, while the MMA work shrinks with M.
+// Here each CTA owns 128 weight columns (one column block) and all M rows:
+// the dequantised weight tile [128 x 64] is the MMA's A operand (M_mma = 128),
+// the x tile [MP x 64] its B operand (N_mma = MP, M rounded up to a multiple
+// of 32), and each CTA's tensor memory holds D[n][m] = y[m][n] for its
+// columns. The weight tile is loaded and dequantised once per CTA and every
+// row of x reuses it (the cooperative shared tile of "ROCm
+// KQuantGemmKWmmaQ4K/Q6K: redesign around a cooperative shared tile",
+// section "Confirmed mechanism"), as in the prefill GEMM, but no tile is
+// padded to 256 rows of x.
+//
+// Warp roles, one CTA per SM, persistent over column blocks:
+//   warp 0      producer: per 64-deep K step, TMA brings the x tile [MP x 64]
+//               (128-byte swizzle, rows >= M zero-filled) and the packed weight
+//               tile [8 words x 128]; the lanes stage the step's scales and
+//               zero-point words with cp.async. One mbarrier per stage.
+//   warps 8-23  two groups of eight on alternate K steps dequantise the packed
+//               tile into the canonical K-major 128-byte-swizzled operand tile:
+//               w = (q - z) * s, (q - z) exact in 16-bit arithmetic, one rounding.
+//   warp 1      one thread issues 4 x tcgen05.mma (kind::f16, M=128, N=MP,
+//               K=16) per step into one of two MP-column FP32 accumulators.
+//   warps 4-7   epilogue: tcgen05.ld of the accumulator (lane = column n,
+//               column = row m of x), round, store y[m][n] (consecutive lanes
+//               write consecutive columns), predicated on m < M and n < N.
+//   warp 2      allocates and frees the tensor memory.
+//
+// Every mbarrier wait is bounded (about two seconds); on expiry the kernel
+// records W4A16_ERR_TIMEOUT in its device word (read by w4a16_device_status),
+// every role stops, the producer and the MMA thread wait (bounded) for their
+// own operations in flight, tensor memory is freed and the kernel returns.
+#include "internal.h"
+#include "ptx.cuh"
+#include "tmap.h"
+
+#include <algorithm>
+
+namespace w4a16 {
+
+__device__ unsigned int g_skinny_error = 0;
+
+namespace {
+
+constexpr int BN = 128, BK = 64;         // weight columns per tile (M of the MMA), K per step
+constexpr int kThreads = 768;
+constexpr int kEpiWarp0 = 4;             // warps 4..7
+constexpr int kDeqWarp0 = 8;             // warps 8..23: two groups taking alternate K steps
+constexpr int kDeqWarps = 8;
+constexpr int kDeqGroups = 2;
+constexpr int kBStages = 4;
+constexpr uint32_t kWBytes = (BK / 8) * BN * 4;      //  4 KB packed weights
+constexpr uint32_t kSBytes = 2 * BN * 2;             // scales of the two 32-row halves of a step
+constexpr uint32_t kZBytes = 2 * (BN / 8) * 4;       // zero-point words of the two halves
+constexpr uint32_t kBBytes = BN * BK * 2;            // 16 KB dequantised operand tile
+constexpr uint32_t kSuspendNs = 20000;
+constexpr unsigned long long kWaitLimitCycles = 4000000000ull;   // ~2 s at 2 GHz
+constexpr unsigned int kErrTimeout = 9u;
+constexpr size_t kSmemBudget = 220 * 1024;
+
+template <int MP>
+struct Cfg {
+    static_assert(MP % 32 == 0 && MP >= 32 && MP <= 256, "rows of x per tile");
+    static constexpr uint32_t kABytes = MP * BK * 2;                                   // x tile
+    static constexpr uint32_t kLoadStageBytes = (kABytes + kWBytes + kSBytes + kZBytes + 1023) & ~1023u;
+    // as many load stages as fit beside the operand ring, an even number (each
+    // dequant group then owns whole load stages: no waiter skips a phase)
+    static constexpr int kRaw = static_cast<int>((kSmemBudget - 2048 - kBStages * kBBytes) / kLoadStageBytes);
+    static constexpr int kLoadStages = (kRaw > 10 ? 10 : kRaw) & ~1;
+    static constexpr uint32_t kAccCols = MP;              // one accumulator
+    static constexpr uint32_t kTmemCols = 2 * MP < 32 ? 32 : 2 * MP;   // two accumulators, power of two
+    static_assert(kLoadStages >= 2, "load ring");
+    static_assert(kLoadStages % kDeqGroups == 0 && kBStages % kDeqGroups == 0,
+                  "each dequant group owns whole ring stages");
+};
+
+template <int MP>
+struct __align__(8) Barriers {
+    uint64_t lfull[Cfg<MP>::kLoadStages];
+    uint64_t lempty[Cfg<MP>::kLoadStages];
+    uint64_t bfull[kBStages];
+    uint64_t bempty[kBStages];
+    uint64_t tfull[2];
+    uint64_t tempty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;
+};
+
+template <int MP>
+constexpr size_t smem_bytes() {
+    return 1024 + Cfg<MP>::kLoadStages * Cfg<MP>::kLoadStageBytes + kBStages * kBBytes + sizeof(Barriers<MP>);
+}
+
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort) {
+    const unsigned long long t0 = clock64();
+    for (;;) {
+        if (mbar_try_wait_suspend(bar, parity, kSuspendNs)) return true;
+        if (*abort) return false;
+        if (clock64() - t0 > kWaitLimitCycles) {
+            *abort = 1;
+            atomicOr(&g_skinny_error, 1u << kErrTimeout);
+            return false;
+        }
+    }
+}
+
+// Lane 0 waits and acquires; the shuffle broadcasts the verdict and orders the
+// other lanes' later accesses after lane 0's acquire.
+__device__ __forceinline__ bool warp_wait_bar(uint32_t bar, uint32_t parity, volatile int* abort, int lane) {
+    int ok = 1;
+    if (lane == 0) ok = wait_bar(bar, parity, abort) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    __syncwarp();
+    return ok != 0;
+}
+
+template <bool kBf16>
+struct Dq;
+template <>
+struct Dq<false> {
+    static constexpr uint32_t kMagic = 0x64006400u;   // fp16 1024.0
+    __device__ static uint32_t sub2(uint32_t a, uint32_t b) {
+        uint32_t d;
+        asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+        return d;
+    }
+    __device__ static uint32_t mul2(uint32_t a, uint32_t b) {
+        uint32_t d;
+        asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+        return d;
+    }
+    __device__ static uint16_t out(float v) { return __half_as_ushort(__float2half_rn(v)); }
+};
+template <>
+struct Dq<true> {
+    static constexpr uint32_t kMagic = 0x43004300u;   // bf16 128.0
+    __device__ static uint32_t sub2(uint32_t a, uint32_t b) {
+        uint32_t d;
+        asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+        return d;
+    }
+    __device__ static uint32_t mul2(uint32_t a, uint32_t b) {
+        uint32_t d;
+        asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+        return d;
+    }
+    __device__ static uint16_t out(float v) { return __bfloat16_as_ushort(__float2bfloat16_rn(v)); }
+};
+
+template <bool kBf16, bool kSym, int MP>
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
+                   const uint16_t* __restrict__ sc, const uint32_t* __restrict__ qz, uint16_t* __restrict__ y, int M,
+                   int N, int K, int g) {
+    using C = Cfg<MP>;
+    constexpr int L = C::kLoadStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* bsmem = smem + L * C::kLoadStageBytes;
+    Barriers<MP>* bars = reinterpret_cast<Barriers<MP>*>(bsmem + kBStages * kBBytes);
+    const uint32_t smem_base = smem_u32(smem);
+    const uint32_t bsmem_base = smem_u32(bsmem);
+    // load stage s: [x tile | packed weights | scales | zero-point words]
+    auto ld_a = [&](int s) { return smem_base + s * C::kLoadStageBytes; };
+    auto ld_w = [&](int s) { return smem + s * C::kLoadStageBytes + C::kABytes; };
+    auto ld_s = [&](int s) { return smem + s * C::kLoadStageBytes + C::kABytes + kWBytes; };
+    auto ld_z = [&](int s) { return smem + s * C::kLoadStageBytes + C::kABytes + kWBytes + kSBytes; };
+    auto op_w = [&](int s) { return bsmem_base + s * kBBytes; };
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tiles = (N + BN - 1) / BN;
+    const int kt_total = (K + BK - 1) / BK;
+    const int groups = K / g;
+    volatile int* abort_flag = &bars->abort;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < L; ++s) {
+            mbar_init(smem_u32(&bars->lfull[s]), 1);
+            mbar_init(smem_u32(&bars->lempty[s]), 1);
+        }
+        for (int s = 0; s < kBStages; ++s) {
+            mbar_init(smem_u32(&bars->bfull[s]), kDeqWarps);
+            mbar_init(smem_u32(&bars->bempty[s]), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(smem_u32(&bars->tfull[a]), 1);
+            mbar_init(smem_u32(&bars->tempty[a]), 4);
+        }
+        mbar_init(smem_u32(&bars->drain), 1);
+        bars->abort = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmap_x);
+        tma_prefetch_desc(&tmap_w);
+    }
+    if (warp == 2) tmem_alloc(smem_u32(&bars->tmem_base), C::kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = bars->tmem_base;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer warp
+        const int half = lane >> 4, sub = lane & 15;
+        int stage = 0;
+        uint32_t phase = 0;
+        uint32_t issued_parity[L];
+        bool issued[L];
+        for (int s = 0; s < L; ++s) issued[s] = false, issued_parity[s] = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+            const int n0 = t * BN;
+            const int n = n0 + 8 * sub;
+            for (int kt = 0; kt < kt_total; ++kt) {
+                if (!warp_wait_bar(smem_u32(&bars->lempty[stage]), phase ^ 1u, abort_flag, lane)) { ok = false; break; }
+                const uint32_t fb = smem_u32(&bars->lfull[stage]);
+                const int grp = (kt * BK + half * (BK / 2)) / g;
+                const bool valid = n < N && grp < groups;
+                const size_t so = valid ? static_cast<size_t>(grp) * N + n : 0;
+                cp_async_16(smem_u32(ld_s(stage)) + half * (BN * 2) + 16 * sub, sc + so, valid ? 16u : 0u);
+                if constexpr (!kSym) {
+                    const size_t zo = valid ? static_cast<size_t>(grp) * (N >> 3) + (n >> 3) : 0;
+                    cp_async_4(smem_u32(ld_z(stage)) + half * (BN / 8) * 4 + 4 * sub, qz + zo, valid ? 4u : 0u);
+                }
+                cp_async_mbar_arrive(fb);
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(fb, C::kABytes + kWBytes);
+                    tma_load_2d(ld_a(stage), &tmap_x, kt * BK, 0, fb);
+                    tma_load_2d(smem_u32(ld_w(stage)), &tmap_w, n0, kt * (BK / 8), fb);
+                }
+                issued[stage] = true;
+                issued_parity[stage] = phase;
+                if (++stage == L) { stage = 0; phase ^= 1u; }
+            }
+        }
+        // copies still in flight must land before this CTA's shared memory is released
+        if (lane == 0) {
+            for (int s = 0; s < L; ++s) {
+                if (!issued[s]) continue;
+                const uint32_t fb = smem_u32(&bars->lfull[s]);
+                const unsigned long long t0 = clock64();
+                while (!mbar_try_wait(fb, issued_parity[s]) && clock64() - t0 < kWaitLimitCycles) {
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t kIdesc = umma_idesc_f16(BN, MP, kBf16);
+            int ls = 0, bs = 0;
+            uint32_t bph = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+                if (!wait_bar(smem_u32(&bars->tempty[acc]), acc_phase ^ 1u, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * C::kAccCols);
+                for (int kt = 0; kt < kt_total; ++kt) {
+                    // completes when the dequant group has written the operand tile,
+                    // which it starts only after the step's x tile has landed
+                    if (!wait_bar(smem_u32(&bars->bfull[bs]), bph, abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint64_t wdesc = sw128_kmajor_desc(op_w(bs));
+                    const uint64_t xdesc = sw128_kmajor_desc(ld_a(ls));
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        umma_f16(d_tmem, wdesc + 2u * kk, xdesc + 2u * kk, kIdesc, (kt | kk) != 0);
+                    umma_commit(smem_u32(&bars->lempty[ls]));
+                    umma_commit(smem_u32(&bars->bempty[bs]));
+                    if (++ls == L) ls = 0;
+                    if (++bs == kBStages) { bs = 0; bph ^= 1u; }
+                }
+                if (!ok) break;
+                umma_commit(smem_u32(&bars->tfull[acc]));
+                if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+            }
+            // every MMA issued by this thread retires before tensor memory is freed
+            umma_commit(smem_u32(&bars->drain));
+            const unsigned long long t0 = clock64();
+            while (!mbar_try_wait(smem_u32(&bars->drain), 0) && clock64() - t0 < kWaitLimitCycles) {
+            }
+        }
+    } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 4) {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;                 // tensor-memory lane quarter: columns 32q .. 32q+31
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
+            if (!warp_wait_bar(smem_u32(&bars->tfull[acc]), acc_phase, abort_flag, lane)) break;
+            tc_fence_after();
+            const int n = t * BN + q * 32 + lane;
+#pragma unroll 1
+            for (int ch = 0; ch < MP / 32; ++ch) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                       static_cast<uint32_t>(acc * C::kAccCols + ch * 32),
+                                   r);
+                tmem_wait_ld();
+                if (n < N) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int m = ch * 32 + i;
+                        if (m < M) y[static_cast<size_t>(m) * N + n] = Dq<kBf16>::out(__uint_as_float(r[i]));
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&bars->tempty[acc]));
+            if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        }
+    } else if (warp >= kDeqWarp0) {
+        // ------------------------------------------------------------ dequantisers
+        const int tg = threadIdx.x - kDeqWarp0 * 32;    // 0..511
+        const int grp = tg >> 8;                         // group: steps j with j % kDeqGroups == grp
+        const int td = tg & 255;
+        const int d = td & (BN - 1);                     // column of the tile
+        const int half = td >> 7;                        // 32-row half of the step: words 4*half .. 4*half+3
+        int ls = 0, bs = 0;
+        uint32_t lph = 0, bph = 0;
+        bool ok = true;
+        int j = 0;
+        auto advance = [&]() {
+            ++j;
+            if (++ls == L) { ls = 0; lph ^= 1u; }
+            if (++bs == kBStages) { bs = 0; bph ^= 1u; }
+        };
+        for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+            for (int kt = 0; kt < kt_total; ++kt) {
+                if (j % kDeqGroups != grp) {
+                    advance();
+                    continue;
+                }
+                if (!warp_wait_bar(smem_u32(&bars->lfull[ls]), lph, abort_flag, lane) ||
+                    !warp_wait_bar(smem_u32(&bars->bempty[bs]), bph ^ 1u, abort_flag, lane)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t* wt = reinterpret_cast<const uint32_t*>(ld_w(ls));
+                const uint16_t* st = reinterpret_cast<const uint16_t*>(ld_s(ls));
+                const uint32_t* zt = reinterpret_cast<const uint32_t*>(ld_z(ls));
+                const uint32_t b_row = op_w(bs) + static_cast<uint32_t>(d) * 128u;
+                const uint32_t s16 = st[half * BN + d];
+                const uint32_t z4 = kSym ? 8u : ((zt[half * (BN / 8) + (d >> 3)] >> (4 * (d & 7))) & 0xFu);
+                const uint32_t ss = s16 | (s16 << 16);
+                const uint32_t zz = Dq<kBf16>::kMagic | z4 | (z4 << 16);
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    const int c = half * 4 + cc;
+                    const uint32_t w = wt[c * BN + d];
+                    const uint32_t w4 = w >> 4;
+                    uint32_t o[4];
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) {
+                        // byte b of w -> low half, byte b of (w >> 4) -> high half:
+                        // halves (magic + q[8c + 2b], magic + q[8c + 2b + 1])
+                        const uint32_t h = and_or(prmt(w, w4, static_cast<uint32_t>(b | ((4 + b) << 8))),
+                                                  0x000F000Fu, Dq<kBf16>::kMagic);
+                        o[b] = Dq<kBf16>::mul2(Dq<kBf16>::sub2(h, zz), ss);
+                    }
+                    const uint32_t dst = b_row + (static_cast<uint32_t>(c ^ (d & 7)) << 4);
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(o[0]), "r"(o[1]),
+                                 "r"(o[2]), "r"(o[3])
+                                 : "memory");
+                }
+                // the MMA (async proxy) reads these writes
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&bars->bfull[bs]));
+                advance();
+            }
+        }
+    }
+
+    __syncwarp();   // single-lane roles (MMA issuer) rejoin their warp
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, C::kTmemCols);
+    }
+}
+
+template <bool kBf16, bool kSym, int MP>
+cudaError_t launch_mp(const void* x, const uint32_t* qw, const void* sc, const uint32_t* qz, void* y, int M, int N,
+                      int K, int g, const DeviceProps& dp, cudaStream_t s) {
+    auto kern = gemm_skinny_kernel<kBf16, kSym, MP>;
+    constexpr size_t kSmem = smem_bytes<MP>();
+    static_assert(kSmem <= 227 * 1024, "shared memory budget");
+    static int configured_device[64] = {0};
+    if (dp.device >= 0 && dp.device < 64 && !configured_device[dp.device]) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmem));
+        if (e != cudaSuccess) return e;
+        configured_device[dp.device] = 1;
+    }
+    CUtensorMap tx, tw;
+    const CUtensorMapDataType adt = kBf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    if (!encode_2d(&tx, adt, x, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, BK, MP, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    if (!encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_INT32, qw, (uint64_t)N, (uint64_t)(K / 8), (uint64_t)N * 4, BN,
+                   BK / 8, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    const int tiles = (N + BN - 1) / BN;
+    const int grid = std::max(1, std::min(tiles, dp.sms));
+    kern<<<grid, kThreads, kSmem, s>>>(tx, tw, static_cast<const uint16_t*>(sc), qz, static_cast<uint16_t*>(y), M, N, K,
+                                       g);
+    return cudaGetLastError();
+}
+
+template <bool kBf16, bool kSym>
+cudaError_t launch_typed(const void* x, const uint32_t* qw, const void* sc, const uint32_t* qz, void* y, int M, int N,
+                         int K, int g, const DeviceProps& dp, cudaStream_t s) {
+    if (M <= 32) return launch_mp<kBf16, kSym, 32>(x, qw, sc, qz, y, M, N, K, g, dp, s);
+    if (M <= 64) return launch_mp<kBf16, kSym, 64>(x, qw, sc, qz, y, M, N, K, g, dp, s);
+    if (M <= 128) return launch_mp<kBf16, kSym, 128>(x, qw, sc, qz, y, M, N, K, g, dp, s);
+    return launch_mp<kBf16, kSym, 256>(x, qw, sc, qz, y, M, N, K, g, dp, s);
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_skinny(const void* x, const uint32_t* qw, const void* sc, const uint32_t* qz, void* y, int M,
+                               int N, int K, int g, bool bf16, const DeviceProps& dp, cudaStream_t s) {
+    if (M < 1 || M > kSkinnyMaxM) return cudaErrorInvalidValue;
+    if (bf16)
+        return qz ? launch_typed<true, false>(x, qw, sc, qz, y, M, N, K, g, dp, s)
+                  : launch_typed<true, true>(x, qw, sc, qz, y, M, N, K, g, dp, s);
+    return qz ? launch_typed<false, false>(x, qw, sc, qz, y, M, N, K, g, dp, s)
+              : launch_typed<false, true>(x, qw, sc, qz, y, M, N, K, g, dp, s);
+}
+
+}  // namespace w4a16
+
+namespace w4a16 {
+cudaError_t read_and_clear_skinny_error(uint32_t* out) {
+    uint32_t v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_skinny_error, sizeof(v));
+    if (e != cudaSuccess) return e;
+    if (v) {
+        const uint32_t zero = 0;
+        e = cudaMemcpyToSymbol(g_skinny_error, &zero, sizeof(zero));
+    }
+    *out = v;
+    return e;
+}
+}  // namespace w4a16

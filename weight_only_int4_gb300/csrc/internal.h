@@ -62,6 +62,17 @@ cudaError_t read_and_clear_device_error(uint32_t* out, cudaStream_t s);
 // Read and clear the device-side error word of the GEMV rings (no sync).
 cudaError_t read_and_clear_gemv_error(uint32_t* out);
 cudaError_t launch_wait_selftest(cudaStream_t s);
+// GEMMs with at most this many rows of x run the operand-swapped kernel
+// (weights as the 128-row MMA operand, x padded to 32..128 rows); measured at
+// N = 43008, K = 5376: 154-160 us for M = 17..128 against 174-180 us on the
+// CTA-pair kernel, which wins from M = 192 on (180 vs 247 us).
+#ifndef W4A16_SKINNY_MAX_M
+#define W4A16_SKINNY_MAX_M 128
+#endif
+constexpr int kSkinnyMaxM = W4A16_SKINNY_MAX_M;
+cudaError_t launch_gemm_skinny(const void* x, const uint32_t* qw, const void* sc, const uint32_t* qz, void* y, int M,
+                               int N, int K, int g, bool bf16, const DeviceProps& dp, cudaStream_t s);
+cudaError_t read_and_clear_skinny_error(uint32_t* out);
 cudaError_t launch_dequant(const uint32_t* qw, const void* sc, const uint32_t* qz, void* out, int N, int K, int g,
                            bool bf16, const DeviceProps& dp, cudaStream_t s);
 
