@@ -27,6 +27,9 @@ import numpy as np
 __all__ = [
     "ACT_DTYPES",
     "Case",
+    "MxCase",
+    "MX_WORKLOADS",
+    "make_mx_case",
     "Workload",
     "WORKLOADS",
     "f32_to_act",
@@ -156,3 +159,68 @@ WORKLOADS = {w.name: w for w in [
 
 def make_case_for(name: str, seed: int = 0) -> Case:
     return WORKLOADS[name].case(seed)
+
+
+# ---------------------------------------------------------------------------
+# MXFP4 weights (E2M1 codes with one E8M0 byte per 32 K rows of a column)
+# ---------------------------------------------------------------------------
+# "Add BF16xFP4 MoE GEMM stage1 kernel" (section "Technical Details") keeps bf16
+# activations and stores weights as E2M1 codes with E8M0 block scales. Codes
+# are uniform on 0..15 (every value of the format, both signs). Exponent
+# bytes: "typical" draws e uniformly on 118..125, i.e. block scales
+# 2^-9..2^-2 and weights of magnitude up to 1.5, the range of trained layer
+# weights; "wide" draws 96..160, so blocks with e > 128 (scales above 2) occur.
+
+
+@dataclass
+class MxCase:
+    """One seeded MXFP4 problem, unpacked.
+
+    x : [M, K] bf16 bit patterns (uint16)
+    q : [K, N] uint8 E2M1 codes, values 0..15
+    e : [K/32, N] uint8 E8M0 exponent bytes
+    """
+
+    M: int
+    N: int
+    K: int
+    x: np.ndarray
+    q: np.ndarray
+    e: np.ndarray
+
+
+_MX_EXPONENTS = {"typical": (118, 125), "wide": (96, 160)}
+
+
+def make_mx_case(M: int, N: int, K: int, seed: int = 0, exponents: str = "typical") -> MxCase:
+    if M < 0 or N < 0 or K < 0 or K % 32:
+        raise ValueError(f"bad MXFP4 shape M={M} N={N} K={K}")
+    lo, hi = _MX_EXPONENTS[exponents]
+    rng = np.random.Generator(np.random.PCG64(seed))
+    x32 = rng.standard_normal((M, K), dtype=np.float32)
+    q = rng.integers(0, 16, size=(K, N), dtype=np.uint8)
+    e = rng.integers(lo, hi + 1, size=(K // 32, N), dtype=np.uint8)
+    return MxCase(M=M, N=N, K=K, x=f32_to_act(x32, "bf16"), q=q, e=e)
+
+
+@dataclass(frozen=True)
+class MxWorkload:
+    """A named MXFP4 problem shape; `kernel` is "gemv", "gemm" or "dequant"."""
+
+    name: str
+    kernel: str
+    M: int
+    N: int
+    K: int
+
+    def case(self, seed: int = 0) -> MxCase:
+        return make_mx_case(self.M, self.N, self.K, seed)
+
+
+# The gate_up layer shape of the W4A16 workloads, with MXFP4 weights.
+MX_WORKLOADS = {w.name: w for w in [
+    MxWorkload("mx_gemv_1x43008x5376_bf16", "gemv", 1, 43008, 5376),
+    MxWorkload("mx_gemm_2048x43008x5376_bf16", "gemm", 2048, 43008, 5376),
+    MxWorkload("mx_gemm_64x43008x5376_bf16", "gemm", 64, 43008, 5376),
+    MxWorkload("mx_dequant_43008x5376_bf16", "dequant", 1, 43008, 5376),
+]}
