@@ -32,8 +32,9 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from w4a16_inputs import WORKLOADS  # noqa: E402
-from weight_only_int4_gb300.accounting import dequant_bytes, layer_bytes, layer_flops  # noqa: E402
+from w4a16_inputs import MX_WORKLOADS, WORKLOADS  # noqa: E402
+from weight_only_int4_gb300.accounting import (dequant_bytes, layer_bytes, layer_flops, mx_dequant_bytes,  # noqa: E402
+                                               mx_layer_bytes)
 
 METRIC = "W4A16 GEMM GB/s (% of HBM peak) at M=1-4; TFLOP/s (% bf16 peak) at M=2048"
 DECODE = "gemv_1x43008x5376_g32_f16_asym"
@@ -175,6 +176,42 @@ class Layer:
             self.fn(x, qw, s, qz, self.wl.g, out=y, workspace=self.ws)
 
 
+class MxLayer:
+    """One MXFP4 workload (E2M1 codes, E8M0 exponents) with `copies` weight sets."""
+
+    def __init__(self, name, copies, torch, w4):
+        self.wl = wl = MX_WORKLOADS[name]
+        case = wl.case(seed=0)
+        self.x = _to_dev(case.x, "bf16", torch)
+        q8 = torch.from_numpy(case.q).cuda()
+        qw = w4.pack(q8, dim=0)
+        del q8
+        e = torch.from_numpy(case.e).cuda()
+        self.weights = [(qw, e)] + [(qw.clone(), e.clone()) for _ in range(copies - 1)]
+        self.fn = getattr(w4, "mxfp4_" + wl.kernel)
+        self.ws = None
+        if wl.kernel == "dequant":
+            self.y = [torch.empty((wl.K, wl.N), dtype=torch.bfloat16, device="cuda") for _ in range(copies)]
+            self.bytes = mx_dequant_bytes(wl.N, wl.K)
+            self.flops = 0
+            return
+        self.y = [torch.empty((wl.M, wl.N), dtype=torch.bfloat16, device="cuda") for _ in range(copies)]
+        if wl.kernel == "gemv":
+            self.ws = w4.new_workspace(w4.workspace_bytes(w4.OP_GEMV, wl.M, wl.N, wl.K, 32))
+        self.bytes = mx_layer_bytes(wl.M, wl.N, wl.K)
+        self.flops = layer_flops(wl.M, wl.N, wl.K)
+
+    def step(self, x=None):
+        x = self.x if x is None else x
+        for (qw, e), y in zip(self.weights, self.y):
+            if self.wl.kernel == "dequant":
+                self.fn(qw, e, out=y)
+            elif self.wl.kernel == "gemv":
+                self.fn(x, qw, e, out=y, workspace=self.ws)
+            else:
+                self.fn(x, qw, e, out=y)
+
+
 def time_graph(layer, steps, warmup, torch, barrier):
     """Device time of `steps` replays of a CUDA graph of one step (events on the replay stream)."""
     stream = torch.cuda.Stream()
@@ -240,6 +277,8 @@ def run_configs(args):
     clocks = ClockSampler(0)
     clocks.start()
     for name, wl in WORKLOADS.items():
+        if args.match and args.match not in name:
+            continue
         per = (dequant_bytes(wl.N, wl.K, wl.g, wl.symmetric, wl.act) if wl.kernel == "dequant" else
                layer_bytes(wl.M, wl.N, wl.K, wl.g, wl.symmetric, wl.act)).total
         L = copies_for(per, l2) if wl.kernel != "gemm" else 2
@@ -248,6 +287,22 @@ def run_configs(args):
         t = [x / L for x in time_graph_samples(layer, steps, max(3, args.warmup), torch)]
         med, mn = statistics.median(t), min(t)
         rows.append({"workload": name, "kernel": wl.kernel, "calls_per_replay": L, "replays": steps,
+                     "us_median": round(med * 1e6, 3), "us_min": round(mn * 1e6, 3),
+                     "GBs": round(per / med / 1e9, 1), "TFLOPs": round(layer.flops / med / 1e12, 2),
+                     "frac_hbm": round(per / med / 1e9 / peaks["hbm_gbs"], 4),
+                     "frac_bf16": round(layer.flops / med / 1e12 / peaks["bf16_tflops"], 4)})
+        del layer
+        torch.cuda.empty_cache()
+    for name, wl in MX_WORKLOADS.items():
+        if args.match and args.match not in name:
+            continue
+        per = (mx_dequant_bytes(wl.N, wl.K) if wl.kernel == "dequant" else mx_layer_bytes(wl.M, wl.N, wl.K)).total
+        L = copies_for(per, l2) if wl.kernel != "gemm" else 2
+        layer = MxLayer(name, L, torch, w4)
+        steps = max(5, args.steps if wl.kernel != "gemm" else args.steps // 10)
+        t = [x / L for x in time_graph_samples(layer, steps, max(3, args.warmup), torch)]
+        med, mn = statistics.median(t), min(t)
+        rows.append({"workload": name, "kernel": "mxfp4_" + wl.kernel, "calls_per_replay": L, "replays": steps,
                      "us_median": round(med * 1e6, 3), "us_min": round(mn * 1e6, 3),
                      "GBs": round(per / med / 1e9, 1), "TFLOPs": round(layer.flops / med / 1e12, 2),
                      "frac_hbm": round(per / med / 1e9 / peaks["hbm_gbs"], 4),
@@ -507,6 +562,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--configs", action="store_true", help="time every named workload (one GPU) and exit")
+    ap.add_argument("--match", default="", help="with --configs: only workloads whose name contains this")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -244,6 +244,58 @@ w4a16_status w4a16_dequant(const int32_t* qweight, const void* scales, const int
                            int64_t K, int64_t g, w4a16_dtype dt, w4a16_stream stream);
 
 /*
+ * MXFP4 weights -- "Add BF16xFP4 MoE GEMM stage1 kernel" (section "Technical
+ * Details"): bf16 activations, weights stored as 4-bit E2M1 codes with one
+ * E8M0 exponent byte e per 32 consecutive K rows of a column, decoded in
+ * software to bf16 before the contraction, FP32 accumulation. The weight is
+ *
+ *     W[k, n] = RN_bf16( E2M1(q[k, n]) * 2^(e[k / 32, n] - 127) )
+ *
+ * where code q has the sign in bit 3, a 2-bit exponent field E (bias 1) in
+ * bits 2..1 and a mantissa bit m in bit 0 (E = 0: m / 2, otherwise
+ * 2^(E - 1) (1 + m/2)): magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6. Byte 0 means
+ * 2^-127 and byte 255 NaN (every weight of that block is NaN). Every W is
+ * exact in bf16 except where it exceeds the bf16 range (+-inf).
+ *
+ * qweight  int32 [K/8, N], the W4A16 word layout: nibble j of word [w, n] is
+ *          the code of row 8w + j
+ * escale   uint8 [K/32, N]: exponent byte of block b, column n at b * N + n
+ * x        bf16 [M, K]; y bf16 [M, N], written (not accumulated into)
+ * Shapes: N % 16 == 0 (each exponent row starts 16-byte aligned), K % 32 == 0.
+ * Every pointer 16-byte aligned device memory owned by the caller.
+ * Errors: NULL, SHAPE, ALIGN, DEVICE, CUDA, WORKSPACE (GEMV only).
+ */
+
+/*
+ * w4a16_mxfp4_dequant -- dense bf16 copy W [K, N] (row-major) of MXFP4
+ * weights. Bit-exact. Streams each operand once; bound by HBM bandwidth.
+ */
+w4a16_status w4a16_mxfp4_dequant(const int32_t* qweight, const uint8_t* escale, void* w, int64_t N, int64_t K,
+                                 w4a16_stream stream);
+
+/*
+ * w4a16_mxfp4_gemv -- decode path for MXFP4 weights, 1 <= M <= 16: the
+ * w4a16_gemv kernel with the E2M1 decode in place of the 4-bit integer one
+ * (each 32-row chunk is one exponent block; its scale 2^(e - 127) is applied
+ * in FP32 once per chunk). Same persistent grid, deterministic fix-up and
+ * programmatic launch. Workspace: at least w4a16_workspace_bytes(W4A16_OP_GEMV,
+ * M, N, K, 32) bytes, with the same ownership and zero-fill rules as for
+ * w4a16_gemv.
+ */
+w4a16_status w4a16_mxfp4_gemv(const void* x, const int32_t* qweight, const uint8_t* escale, void* y, int64_t M,
+                              int64_t N, int64_t K, void* workspace, size_t workspace_bytes,
+                              w4a16_stream stream);
+
+/*
+ * w4a16_mxfp4_gemm -- prefill path for MXFP4 weights, any M >= 1: the
+ * w4a16_gemm kernels (operand-swapped for M <= 128, CTA pairs above) with the
+ * E2M1 decode writing the bf16 operand tile. A pipeline wait that runs out
+ * sets the device flag that w4a16_device_status reports.
+ */
+w4a16_status w4a16_mxfp4_gemm(const void* x, const int32_t* qweight, const uint8_t* escale, void* y, int64_t M,
+                              int64_t N, int64_t K, w4a16_stream stream);
+
+/*
  * w4a16_device_status -- synchronise `stream`, then read and clear the
  * device-side error word of the current device. Every wait on an mbarrier
  * inside the GEMM pipeline gives up after about two seconds; the kernel then

@@ -23,7 +23,7 @@ def lib():
 def declared_symbols():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(w4a16_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(w4a16_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_header_declares_the_binding_table():
@@ -121,6 +121,38 @@ def _has_cuda_device():
 
 
 @pytest.mark.skipif(_has_cuda_device(), reason="needs a host without a CUDA device")
+def _mx(lib, fn, **kw):
+    a = dict(x=P, qw=P, e=P, y=P, M=1, N=64, K=128)
+    a.update(kw)
+    if fn == "dequant":
+        return lib.w4a16_mxfp4_dequant(a["qw"], a["e"], a["y"], a["N"], a["K"], None)
+    if fn == "gemv":
+        return lib.w4a16_mxfp4_gemv(a["x"], a["qw"], a["e"], a["y"], a["M"], a["N"], a["K"], a.get("ws", P),
+                                    a.get("ws_bytes", 1 << 30), None)
+    return lib.w4a16_mxfp4_gemm(a["x"], a["qw"], a["e"], a["y"], a["M"], a["N"], a["K"], None)
+
+
+@pytest.mark.parametrize("fn", ["dequant", "gemv", "gemm"])
+def test_mxfp4_rejections(lib, fn):
+    assert _mx(lib, fn, qw=0) == w4.ERR_NULL
+    assert _mx(lib, fn, e=0) == w4.ERR_NULL
+    assert _mx(lib, fn, y=0) == w4.ERR_NULL
+    assert _mx(lib, fn, N=8) == w4.ERR_SHAPE           # exponent rows must start 16-byte aligned
+    assert _mx(lib, fn, K=48) == w4.ERR_SHAPE          # K % 32
+    assert _mx(lib, fn, K=0) == w4.ERR_SHAPE
+    assert _mx(lib, fn, e=MIS) == w4.ERR_ALIGN
+    assert _mx(lib, fn, qw=MIS) == w4.ERR_ALIGN
+    assert _mx(lib, fn, y=MIS) == w4.ERR_ALIGN
+    if fn != "dequant":
+        assert _mx(lib, fn, x=0) == w4.ERR_NULL
+        assert _mx(lib, fn, M=0) == w4.ERR_SHAPE
+        assert _mx(lib, fn, x=MIS) == w4.ERR_ALIGN
+    if fn == "gemv":
+        assert _mx(lib, fn, M=17) == w4.ERR_SHAPE
+        assert _mx(lib, fn, ws=0) == w4.ERR_WORKSPACE
+        assert _mx(lib, fn, ws=MIS) == w4.ERR_WORKSPACE
+
+
 def test_valid_arguments_stop_at_the_device_gate(lib):
     assert _gemv(lib) == w4.ERR_DEVICE
     assert _gemm(lib) == w4.ERR_DEVICE
@@ -128,6 +160,9 @@ def test_valid_arguments_stop_at_the_device_gate(lib):
     assert lib.w4a16_device_status(None) == w4.ERR_DEVICE
     assert lib.w4a16_selftest_wait_timeout(None) == w4.ERR_DEVICE
     assert lib.w4a16_dequant(P, P, P, P, 64, 128, 32, w4.F16, None) == w4.ERR_DEVICE
+    for fn in ("dequant", "gemv", "gemm"):
+        assert _mx(lib, fn) == w4.ERR_DEVICE
+    assert _mx(lib, "gemm", M=4096) == w4.ERR_DEVICE
     assert lib.w4a16_workspace_bytes(w4.OP_GEMV, 1, 64, 128, 32) == 0
 
 

@@ -2,7 +2,8 @@
 "Keep W4A16 zero-points packed at 4 bits instead of expanding to 2 bytes"."""
 import pytest
 
-from weight_only_int4_gb300.accounting import expanded_zero_bytes, layer_bytes, layer_flops
+from weight_only_int4_gb300.accounting import (expanded_zero_bytes, layer_bytes, layer_flops, mx_dequant_bytes,
+                                                mx_layer_bytes)
 
 
 def _rows(golden):
@@ -45,3 +46,11 @@ def test_symmetric_has_no_zero_bytes():
 
 def test_flops():
     assert layer_flops(2048, 43008, 5376) == 947_040_288_768
+
+
+def test_mxfp4_bytes():
+    b = mx_layer_bytes(1, 43008, 5376)
+    assert b.weights == 43008 * 5376 // 2 and b.scales == 168 * 43008 and b.zeros == 0
+    assert b.total == 43008 * 5376 // 2 + 168 * 43008 + 5376 * 2 + 43008 * 2
+    d = mx_dequant_bytes(43008, 5376)
+    assert d.x == 0 and d.y == 43008 * 5376 * 2 and d.operands == b.operands

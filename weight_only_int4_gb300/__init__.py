@@ -53,6 +53,9 @@ SIGNATURES = {
     "w4a16_device_status": (_INT, [_VP]),
     "w4a16_selftest_wait_timeout": (_INT, [_VP]),
     "w4a16_dequant": (_INT, [_VP, _VP, _VP, _VP, _I64, _I64, _I64, _INT, _VP]),
+    "w4a16_mxfp4_dequant": (_INT, [_VP, _VP, _VP, _I64, _I64, _VP]),
+    "w4a16_mxfp4_gemv": (_INT, [_VP, _VP, _VP, _VP, _I64, _I64, _I64, _VP, _SZ, _VP]),
+    "w4a16_mxfp4_gemm": (_INT, [_VP, _VP, _VP, _VP, _I64, _I64, _I64, _VP]),
     "w4a16_status_string": (ctypes.c_char_p, [_INT]),
     "w4a16_abi_version": (_INT, []),
 }
@@ -267,6 +270,77 @@ def dequant(qweight, scales, qzeros: Optional[object], group_size: int, out=None
         raise ValueError(f"out must be {scales.dtype} [K, N] = [{K}, {N}]")
     _check("w4a16_dequant", load_library().w4a16_dequant(qweight.data_ptr(), scales.data_ptr(), zp, out.data_ptr(),
                                                          N, K, group_size, dt, _stream_ptr(stream)))
+    return out
+
+
+def _mx_weights(qweight, escale):
+    torch = _torch()
+    for name, t in (("qweight", qweight), ("escale", escale)):
+        _cuda_contig(name, t)
+    if qweight.dim() != 2 or escale.dim() != 2:
+        raise ValueError("qweight and escale must be 2-D")
+    if qweight.dtype != torch.int32:
+        raise TypeError(f"qweight must be torch.int32, got {qweight.dtype}")
+    if escale.dtype != torch.uint8:
+        raise TypeError(f"escale must be torch.uint8 E8M0 bytes, got {escale.dtype}")
+    K, N = qweight.shape[0] * 8, qweight.shape[1]
+    if escale.shape != (K // 32, N) or K % 32:
+        raise ValueError(f"escale shape {tuple(escale.shape)} does not match (K/32, N)")
+    return K, N
+
+
+def _mx_layer(fn_name: str, x, qweight, escale, out, workspace, stream):
+    torch = _torch()
+    K, N = _mx_weights(qweight, escale)
+    _cuda_contig("x", x)
+    if x.dim() != 2 or x.dtype != torch.bfloat16:
+        raise TypeError("x must be a 2-D torch.bfloat16 tensor")
+    M = x.shape[0]
+    if x.shape[1] != K:
+        raise ValueError(f"x has {x.shape[1]} columns, qweight holds K = {K} rows")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    _cuda_contig("out", out)
+    if out.shape != (M, N) or out.dtype != torch.bfloat16:
+        raise ValueError(f"out must be bf16 [M, N] = [{M}, {N}]")
+    lib = load_library()
+    sp = _stream_ptr(stream)
+    if fn_name == "w4a16_mxfp4_gemm":
+        _check(fn_name, lib.w4a16_mxfp4_gemm(x.data_ptr(), qweight.data_ptr(), escale.data_ptr(), out.data_ptr(),
+                                              M, N, K, sp))
+        return out
+    if workspace is None:
+        need = lib.w4a16_workspace_bytes(OP_GEMV, M, N, K, 32)
+        workspace = _cached_workspace(need, x.device, sp) if need else None
+    ws_ptr, ws_bytes = (0, 0) if workspace is None else (workspace.data_ptr(),
+                                                          workspace.numel() * workspace.element_size())
+    _check(fn_name, lib.w4a16_mxfp4_gemv(x.data_ptr(), qweight.data_ptr(), escale.data_ptr(), out.data_ptr(),
+                                          M, N, K, ws_ptr, ws_bytes, sp))
+    return out
+
+
+def mxfp4_gemv(x, qweight, escale, out=None, workspace=None, stream=None):
+    """Decode path for MXFP4 weights (E2M1 codes in `qweight`, E8M0 bytes
+    `escale` [K/32, N]); x bf16 [M, K] with 1 <= M <= 16. Returns bf16 y [M, N]."""
+    return _mx_layer("w4a16_mxfp4_gemv", x, qweight, escale, out, workspace, stream)
+
+
+def mxfp4_gemm(x, qweight, escale, out=None, stream=None):
+    """Prefill path for MXFP4 weights (any M >= 1, tcgen05). Returns bf16 y [M, N]."""
+    return _mx_layer("w4a16_mxfp4_gemm", x, qweight, escale, out, None, stream)
+
+
+def mxfp4_dequant(qweight, escale, out=None, stream=None):
+    """Dense bf16 copy W[k, n] = E2M1(q[k, n]) * 2^(e[k/32, n] - 127), [K, N]."""
+    torch = _torch()
+    K, N = _mx_weights(qweight, escale)
+    if out is None:
+        out = torch.empty((K, N), dtype=torch.bfloat16, device=qweight.device)
+    _cuda_contig("out", out)
+    if out.shape != (K, N) or out.dtype != torch.bfloat16:
+        raise ValueError(f"out must be bf16 [K, N] = [{K}, {N}]")
+    _check("w4a16_mxfp4_dequant", load_library().w4a16_mxfp4_dequant(qweight.data_ptr(), escale.data_ptr(),
+                                                                       out.data_ptr(), N, K, _stream_ptr(stream)))
     return out
 
 

@@ -57,5 +57,18 @@ def expanded_zero_bytes(N: int, K: int, g: int, act: str = "f16") -> int:
     return (K // g) * N * ACT_BYTES[act]
 
 
+def mx_layer_bytes(M: int, N: int, K: int) -> LayerBytes:
+    """MXFP4 weights ("Add BF16xFP4 MoE GEMM stage1 kernel", section
+    "Technical Details"): 4-bit codes, one E8M0 byte per 32 K rows of a
+    column, no zero-points; bf16 x and y."""
+    return LayerBytes(weights=K * N // 2, scales=(K // 32) * N, zeros=0, x=M * K * 2, y=M * N * 2)
+
+
+def mx_dequant_bytes(N: int, K: int) -> LayerBytes:
+    """The dense bf16 copy of MXFP4 weights: reads codes and exponents once, writes K x N bf16."""
+    b = mx_layer_bytes(1, N, K)
+    return LayerBytes(weights=b.weights, scales=b.scales, zeros=0, x=0, y=K * N * 2)
+
+
 def layer_flops(M: int, N: int, K: int) -> int:
     return 2 * M * N * K

@@ -78,6 +78,27 @@ w4a16_status check_layer_args(const void* x, const int32_t* qweight, const void*
     return W4A16_OK;
 }
 
+// MXFP4 weights: qweight int32 [K/8, N]; exponent bytes [K/32, N] (N % 16:
+// every row of the byte tensor starts 16-byte aligned).
+w4a16_status check_mx_weights(const int32_t* qweight, const uint8_t* escale, int64_t N, int64_t K) {
+    if (!qweight || !escale) return W4A16_ERR_NULL;
+    if (N < 1 || K < 1 || N > kMaxDim || K > kMaxDim) return W4A16_ERR_SHAPE;
+    if (N % 16 != 0 || K % 32 != 0) return W4A16_ERR_SHAPE;
+    if (!aligned16(qweight) || !aligned16(escale)) return W4A16_ERR_ALIGN;
+    return W4A16_OK;
+}
+
+// ... and bf16 x [M, K], y [M, N]
+w4a16_status check_mx_args(const void* x, const int32_t* qweight, const uint8_t* escale, const void* y, int64_t M,
+                           int64_t N, int64_t K, int64_t max_m) {
+    if (!x || !y) return W4A16_ERR_NULL;
+    w4a16_status st = check_mx_weights(qweight, escale, N, K);
+    if (st != W4A16_OK) return st;
+    if (M < 1 || M > kMaxDim || (max_m > 0 && M > max_m)) return W4A16_ERR_SHAPE;
+    if (!aligned16(x) || !aligned16(y)) return W4A16_ERR_ALIGN;
+    return W4A16_OK;
+}
+
 w4a16_status from_cuda(cudaError_t e) { return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA; }
 
 }  // namespace
@@ -211,6 +232,44 @@ w4a16_status w4a16_dequant(const int32_t* qweight, const void* scales, const int
     return from_cuda(w4a16::launch_dequant(reinterpret_cast<const uint32_t*>(qweight), scales,
                                            reinterpret_cast<const uint32_t*>(qzeros), w, (int)N, (int)K, (int)g,
                                            dt == W4A16_BF16, dp, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+w4a16_status w4a16_mxfp4_dequant(const int32_t* qweight, const uint8_t* escale, void* w, int64_t N, int64_t K,
+                                 w4a16_stream stream) {
+    if (!w) return W4A16_ERR_NULL;
+    w4a16_status st = check_mx_weights(qweight, escale, N, K);
+    if (st != W4A16_OK) return st;
+    if (!aligned16(w)) return W4A16_ERR_ALIGN;
+    DeviceProps dp;
+    if ((st = device_gate(&dp)) != W4A16_OK) return st;
+    return from_cuda(w4a16::launch_mx_dequant(reinterpret_cast<const uint32_t*>(qweight), escale, w, (int)N, (int)K,
+                                              dp, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+w4a16_status w4a16_mxfp4_gemv(const void* x, const int32_t* qweight, const uint8_t* escale, void* y, int64_t M,
+                              int64_t N, int64_t K, void* workspace, size_t workspace_bytes, w4a16_stream stream) {
+    w4a16_status st = check_mx_args(x, qweight, escale, y, M, N, K, 16);
+    if (st != W4A16_OK) return st;
+    if (!workspace || !aligned16(workspace)) return W4A16_ERR_WORKSPACE;
+    DeviceProps dp;
+    if ((st = device_gate(&dp)) != W4A16_OK) return st;
+    const w4a16::GemvPlan plan = w4a16::plan_mx_gemv((int)M, (int)N, (int)K, dp);
+    if (workspace_bytes < w4a16::gemv_workspace_bytes(plan)) return W4A16_ERR_WORKSPACE;
+    return from_cuda(w4a16::launch_mx_gemv(x, reinterpret_cast<const uint32_t*>(qweight), escale, y, (int)M, (int)N,
+                                           (int)K, plan, workspace, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+w4a16_status w4a16_mxfp4_gemm(const void* x, const int32_t* qweight, const uint8_t* escale, void* y, int64_t M,
+                              int64_t N, int64_t K, w4a16_stream stream) {
+    w4a16_status st = check_mx_args(x, qweight, escale, y, M, N, K, 0);
+    if (st != W4A16_OK) return st;
+    DeviceProps dp;
+    if ((st = device_gate(&dp)) != W4A16_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const uint32_t* qw = reinterpret_cast<const uint32_t*>(qweight);
+    if (M <= w4a16::kSkinnyMaxM)
+        return from_cuda(w4a16::launch_mx_gemm_skinny(x, qw, escale, y, (int)M, (int)N, (int)K, dp, s));
+    return from_cuda(w4a16::launch_mx_gemm(x, qw, escale, y, (int)M, (int)N, (int)K, dp, s));
 }
 
 w4a16_status w4a16_selftest_wait_timeout(w4a16_stream stream) {

@@ -17,6 +17,7 @@
 // 128 (bf16) turns them into magic + q, one packed subtract of magic + z gives
 // the exact (q - z), one packed multiply by s rounds once.
 #include "internal.h"
+#include "mxfp4.cuh"
 #include "ptx.cuh"
 
 #include <algorithm>
@@ -121,7 +122,56 @@ cudaError_t launch_typed(const uint32_t* qw, const void* sc, const uint32_t* qz,
     return cudaGetLastError();
 }
 
+// MXFP4 weights to a dense bf16 copy, W[k, n] = RN(E2M1(q[k, n]) * 2^(e[k / 32, n] - 127)).
+// Same thread layout as above: one packed word row of 8 adjacent columns, with
+// the 8 exponent bytes of its 32-row block in one 8-byte load.
+__global__ void __launch_bounds__(kThreads) mx_dequant_kernel(const uint32_t* __restrict__ qw,
+                                                             const uint8_t* __restrict__ es,
+                                                             uint16_t* __restrict__ out, int N, long long items) {
+    const int ng = N >> 3;
+    for (long long i = blockIdx.x * static_cast<long long>(kThreads) + threadIdx.x; i < items;
+         i += static_cast<long long>(gridDim.x) * kThreads) {
+        const long long w = i / ng;
+        const int c = static_cast<int>(i - w * ng);
+        const long long blk = (w * 8) / mx::kBlock;
+        const uint4 q0 = ld_stream(qw + w * N + 8 * c);
+        const uint4 q1 = ld_stream(qw + w * N + 8 * c + 4);
+        const uint2 e8 = __ldg(reinterpret_cast<const uint2*>(es + blk * N + 8 * c));
+        uint32_t fa[4], fb[4];
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            const uint32_t ew = p < 2 ? e8.x : e8.y;
+            const int sh = 16 * (p & 1);
+            mx::pair_factors((ew >> sh) & 0xFFu, (ew >> (sh + 8)) & 0xFFu, fa[p], fb[p]);
+        }
+        uint32_t wd[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+        uint16_t* orow = out + (w * 8) * static_cast<long long>(N) + 8 * c;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            uint32_t o[4];
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                // code j of columns 2p and 2p+1 in bits 0-3 of the two halves
+                const uint32_t h = prmt(wd[2 * p], wd[2 * p + 1], 0x5410u) & 0x000F000Fu;
+                o[p] = mx::mul_bf16x2(mx::mul_bf16x2(mx::e2m1x2_scaled(h), fa[p]), fb[p]);
+            }
+            st_stream(orow + static_cast<long long>(j) * N, o[0], o[1], o[2], o[3]);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) wd[u] >>= 4;
+        }
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_mx_dequant(const uint32_t* qw, const uint8_t* es, void* out, int N, int K, const DeviceProps& dp,
+                              cudaStream_t s) {
+    const long long items = static_cast<long long>(K / 8) * (N / 8);
+    const long long want = (items + kThreads - 1) / kThreads;
+    const int grid = static_cast<int>(std::min<long long>(want, static_cast<long long>(dp.sms) * 8));
+    mx_dequant_kernel<<<grid, kThreads, 0, s>>>(qw, es, static_cast<uint16_t*>(out), N, items);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_dequant(const uint32_t* qw, const void* sc, const uint32_t* qz, void* out, int N, int K, int g,
                            bool bf16, const DeviceProps& dp, cudaStream_t s) {

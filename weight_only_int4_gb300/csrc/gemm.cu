@@ -48,6 +48,7 @@
 // their own operations in flight, the pair synchronises, tensor memory is
 // freed and the kernel returns.
 #include "internal.h"
+#include "mxfp4.cuh"
 #include "ptx.cuh"
 
 #include "tmap.h"
@@ -217,7 +218,9 @@ struct Deq<true> {
     }
 };
 
-template <bool kBf16, bool kSym>
+// kMx: MXFP4 weights (bf16 only): `sc` holds the E8M0 bytes [K/32, N] and
+// there are no zero-points; every 32-row half of a K step is one scale block.
+template <bool kBf16, bool kSym, bool kMx = false>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
             const uint16_t* __restrict__ sc, const uint32_t* __restrict__ qz, uint16_t* __restrict__ y, int M,
@@ -296,7 +299,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
                 const int grp = (kt * BK + half * (BK / 2)) / g;
                 const bool valid = n < N && grp < groups;
                 const size_t so = valid ? static_cast<size_t>(grp) * N + n : 0;
-                cp_async_16(smem_u32(ld_s(stage)) + half * (CN * 2) + 16 * sub, sc + so, valid ? 16u : 0u);
+                if constexpr (kMx) {
+                    // 8 exponent bytes of the lane's columns for this 32-row block
+                    cp_async_8(smem_u32(ld_s(stage)) + half * CN + 8 * sub,
+                               reinterpret_cast<const uint8_t*>(sc) + so, valid ? 8u : 0u);
+                } else {
+                    cp_async_16(smem_u32(ld_s(stage)) + half * (CN * 2) + 16 * sub, sc + so, valid ? 16u : 0u);
+                }
                 if constexpr (!kSym) {
                     const size_t zo = valid ? static_cast<size_t>(grp) * (N >> 3) + (n >> 3) : 0;
                     cp_async_4(smem_u32(ld_z(stage)) + half * (CN / 8) * 4 + 4 * sub, qz + zo, valid ? 4u : 0u);
@@ -458,6 +467,14 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
                 const uint16_t* st = reinterpret_cast<const uint16_t*>(ld_s(ls));
                 const uint32_t* zt = reinterpret_cast<const uint32_t*>(ld_z(ls));
                 const uint32_t b_row = op_b(bs) + static_cast<uint32_t>(d) * 128u;
+                if constexpr (kMx) {
+                    mx::operand_column<CN>(wt, b_row, d, half, reinterpret_cast<const uint8_t*>(st)[half * CN + d]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(rank == 0 ? &bars->bfull[bs] : &bars->bready[bs]));
+                    advance();
+                    continue;
+                }
                 const uint32_t s16 = st[half * CN + d];
                 const uint32_t z4 = kSym ? 8u : ((zt[half * (CN / 8) + (d >> 3)] >> (4 * (d & 7))) & 0xFu);
                 const uint32_t ss = s16 | (s16 << 16);
@@ -506,7 +523,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
 // ---------------------------------------------------------------------------
 // Clusters of two CTAs that can be resident at once (one CTA per SM; a GPC
 // with an odd number of free SMs leaves one idle), per device.
-template <bool kBf16, bool kSym>
+template <bool kBf16, bool kSym, bool kMx>
 int resident_pairs(const DeviceProps& dp) {
     static std::mutex mu;
     static int cached[64] = {0};
@@ -525,7 +542,7 @@ int resident_pairs(const DeviceProps& dp) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, gemm_kernel<kBf16, kSym>, &cfg) != cudaSuccess || n <= 0) {
+        if (cudaOccupancyMaxActiveClusters(&n, gemm_kernel<kBf16, kSym, kMx>, &cfg) != cudaSuccess || n <= 0) {
             (void)cudaGetLastError();
             n = dp.sms / 2;
         }
@@ -534,10 +551,10 @@ int resident_pairs(const DeviceProps& dp) {
     return cached[dev];
 }
 
-template <bool kBf16, bool kSym>
+template <bool kBf16, bool kSym, bool kMx = false>
 cudaError_t launch_typed(const void* x, const uint32_t* qw, const void* sc, const uint32_t* qz, void* y, int M,
                          int N, int K, int g, const DeviceProps& dp, cudaStream_t s) {
-    auto kern = gemm_kernel<kBf16, kSym>;
+    auto kern = gemm_kernel<kBf16, kSym, kMx>;
     static int configured_device[64] = {0};
     if (dp.device >= 0 && dp.device < 64 && !configured_device[dp.device]) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -554,7 +571,7 @@ cudaError_t launch_typed(const void* x, const uint32_t* qw, const void* sc, cons
                    (uint64_t)N * 4, CN, BK / 8, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
     const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
-    const int pairs = std::max(1, std::min(tiles, resident_pairs<kBf16, kSym>(dp)));
+    const int pairs = std::max(1, std::min(tiles, resident_pairs<kBf16, kSym, kMx>(dp)));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * pairs);
     cfg.blockDim = dim3(kThreads);
@@ -580,6 +597,11 @@ cudaError_t launch_gemm(const void* x, const uint32_t* qw, const void* sc, const
                   : launch_typed<true, true>(x, qw, sc, qz, y, M, N, K, g, dp, s);
     return qz ? launch_typed<false, false>(x, qw, sc, qz, y, M, N, K, g, dp, s)
               : launch_typed<false, true>(x, qw, sc, qz, y, M, N, K, g, dp, s);
+}
+
+cudaError_t launch_mx_gemm(const void* x, const uint32_t* qw, const uint8_t* es, void* y, int M, int N, int K,
+                           const DeviceProps& dp, cudaStream_t s) {
+    return launch_typed<true, true, true>(x, qw, es, nullptr, y, M, N, K, mx::kBlock, dp, s);
 }
 
 cudaError_t read_and_clear_device_error(uint32_t* out, cudaStream_t s) {

@@ -33,6 +33,7 @@
 // every role stops, the producer and the MMA thread wait (bounded) for their
 // own operations in flight, tensor memory is freed and the kernel returns.
 #include "internal.h"
+#include "mxfp4.cuh"
 #include "ptx.cuh"
 #include "tmap.h"
 
@@ -150,7 +151,9 @@ struct Dq<true> {
     __device__ static uint16_t out(float v) { return __bfloat16_as_ushort(__float2bfloat16_rn(v)); }
 };
 
-template <bool kBf16, bool kSym, int MP>
+// kMx: MXFP4 weights (bf16 only): `sc` holds the E8M0 bytes [K/32, N] and
+// there are no zero-points; every 32-row half of a K step is one scale block.
+template <bool kBf16, bool kSym, int MP, bool kMx = false>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
                    const uint16_t* __restrict__ sc, const uint32_t* __restrict__ qz, uint16_t* __restrict__ y, int M,
@@ -219,7 +222,12 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_cons
                 const int grp = (kt * BK + half * (BK / 2)) / g;
                 const bool valid = n < N && grp < groups;
                 const size_t so = valid ? static_cast<size_t>(grp) * N + n : 0;
-                cp_async_16(smem_u32(ld_s(stage)) + half * (BN * 2) + 16 * sub, sc + so, valid ? 16u : 0u);
+                if constexpr (kMx) {
+                    cp_async_8(smem_u32(ld_s(stage)) + half * BN + 8 * sub, reinterpret_cast<const uint8_t*>(sc) + so,
+                               valid ? 8u : 0u);
+                } else {
+                    cp_async_16(smem_u32(ld_s(stage)) + half * (BN * 2) + 16 * sub, sc + so, valid ? 16u : 0u);
+                }
                 if constexpr (!kSym) {
                     const size_t zo = valid ? static_cast<size_t>(grp) * (N >> 3) + (n >> 3) : 0;
                     cp_async_4(smem_u32(ld_z(stage)) + half * (BN / 8) * 4 + 4 * sub, qz + zo, valid ? 4u : 0u);
@@ -344,6 +352,14 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_cons
                 const uint16_t* st = reinterpret_cast<const uint16_t*>(ld_s(ls));
                 const uint32_t* zt = reinterpret_cast<const uint32_t*>(ld_z(ls));
                 const uint32_t b_row = op_w(bs) + static_cast<uint32_t>(d) * 128u;
+                if constexpr (kMx) {
+                    mx::operand_column<BN>(wt, b_row, d, half, reinterpret_cast<const uint8_t*>(st)[half * BN + d]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&bars->bfull[bs]));
+                    advance();
+                    continue;
+                }
                 const uint32_t s16 = st[half * BN + d];
                 const uint32_t z4 = kSym ? 8u : ((zt[half * (BN / 8) + (d >> 3)] >> (4 * (d & 7))) & 0xFu);
                 const uint32_t ss = s16 | (s16 << 16);
@@ -385,10 +401,10 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_cons
     }
 }
 
-template <bool kBf16, bool kSym, int MP>
+template <bool kBf16, bool kSym, int MP, bool kMx = false>
 cudaError_t launch_mp(const void* x, const uint32_t* qw, const void* sc, const uint32_t* qz, void* y, int M, int N,
                       int K, int g, const DeviceProps& dp, cudaStream_t s) {
-    auto kern = gemm_skinny_kernel<kBf16, kSym, MP>;
+    auto kern = gemm_skinny_kernel<kBf16, kSym, MP, kMx>;
     constexpr size_t kSmem = smem_bytes<MP>();
     static_assert(kSmem <= 227 * 1024, "shared memory budget");
     static int configured_device[64] = {0};
@@ -411,13 +427,13 @@ cudaError_t launch_mp(const void* x, const uint32_t* qw, const void* sc, const u
     return cudaGetLastError();
 }
 
-template <bool kBf16, bool kSym>
+template <bool kBf16, bool kSym, bool kMx = false>
 cudaError_t launch_typed(const void* x, const uint32_t* qw, const void* sc, const uint32_t* qz, void* y, int M, int N,
                          int K, int g, const DeviceProps& dp, cudaStream_t s) {
-    if (M <= 32) return launch_mp<kBf16, kSym, 32>(x, qw, sc, qz, y, M, N, K, g, dp, s);
-    if (M <= 64) return launch_mp<kBf16, kSym, 64>(x, qw, sc, qz, y, M, N, K, g, dp, s);
-    if (M <= 128) return launch_mp<kBf16, kSym, 128>(x, qw, sc, qz, y, M, N, K, g, dp, s);
-    return launch_mp<kBf16, kSym, 256>(x, qw, sc, qz, y, M, N, K, g, dp, s);
+    if (M <= 32) return launch_mp<kBf16, kSym, 32, kMx>(x, qw, sc, qz, y, M, N, K, g, dp, s);
+    if (M <= 64) return launch_mp<kBf16, kSym, 64, kMx>(x, qw, sc, qz, y, M, N, K, g, dp, s);
+    if (M <= 128) return launch_mp<kBf16, kSym, 128, kMx>(x, qw, sc, qz, y, M, N, K, g, dp, s);
+    return launch_mp<kBf16, kSym, 256, kMx>(x, qw, sc, qz, y, M, N, K, g, dp, s);
 }
 
 }  // namespace
@@ -430,6 +446,12 @@ cudaError_t launch_gemm_skinny(const void* x, const uint32_t* qw, const void* sc
                   : launch_typed<true, true>(x, qw, sc, qz, y, M, N, K, g, dp, s);
     return qz ? launch_typed<false, false>(x, qw, sc, qz, y, M, N, K, g, dp, s)
               : launch_typed<false, true>(x, qw, sc, qz, y, M, N, K, g, dp, s);
+}
+
+cudaError_t launch_mx_gemm_skinny(const void* x, const uint32_t* qw, const uint8_t* es, void* y, int M, int N, int K,
+                                  const DeviceProps& dp, cudaStream_t s) {
+    if (M < 1 || M > kSkinnyMaxM) return cudaErrorInvalidValue;
+    return launch_typed<true, true, true>(x, qw, es, nullptr, y, M, N, K, mx::kBlock, dp, s);
 }
 
 }  // namespace w4a16

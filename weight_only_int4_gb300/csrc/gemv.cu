@@ -35,6 +35,7 @@
 //     contributing CTAs in ascending CTA order, so the result is deterministic,
 //     and resets the ticket to zero for the next call.
 #include "internal.h"
+#include "mxfp4.cuh"
 #include "ptx.cuh"
 #include "tmap.h"
 
@@ -139,6 +140,8 @@ __device__ __forceinline__ void lds(uint32_t addr, uint32_t (&v)[(BYTES + 3) / 4
         asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v[0]), "=r"(v[1]) : "r"(addr));
     else if constexpr (BYTES == 4)
         asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v[0]) : "r"(addr));
+    else if constexpr (BYTES == 1)
+        asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v[0]) : "r"(addr));
     else {
         uint16_t h;
         asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h) : "r"(addr));
@@ -169,7 +172,7 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int lan
 
 struct GemvArgs {
     CUtensorMap tq;       // qweight int32 [K/8, N], box [4 rows, CB]
-    CUtensorMap ts;       // scales 16-bit [K/g, N], box [1, CB]
+    CUtensorMap ts;       // scales 16-bit [K/g, N] (MXFP4: exponent bytes [K/32, N]), box [1, CB]
     CUtensorMap tz;       // qzeros int32 [K/g, N/8], box [1, CB/8] (used when N % 32 == 0)
     CUtensorMap tx;       // x 16-bit [M, K], box [MT rows, 32]
     const uint32_t* qz;
@@ -203,8 +206,16 @@ __device__ __forceinline__ int owner_cta(long long i, long long T, int G) {
 }
 __device__ __forceinline__ long long range_start(int b, long long T, int G) { return (long long)b * T / G; }
 
-template <bool kBf16, int MT, int COLS, bool kSym, bool kFact, bool kZBulk>
+// kMx: MXFP4 weights (bf16, with kSym and without kFact or kZBulk): each
+// 32-row chunk is one E8M0 block. The warp first rewrites the chunk's bf16 x
+// slice in place as fp16 scaled by a power of two per row (mx::x_to_f16);
+// codes become fp16 pairs in one conversion instruction each, the products
+// are exact in an FP32 FMA with fp16 inputs, and the power of two and the
+// block scale 2^(e - 127) are applied in FP32 once per chunk.
+template <bool kBf16, int MT, int COLS, bool kSym, bool kFact, bool kZBulk, bool kMx = false>
 __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant__ GemvArgs a) {
+    static_assert(!kMx || (kBf16 && kSym && !kFact && !kZBulk), "MXFP4: bf16, no zero-points");
+    static_assert(!kMx || Stage<COLS, MT>::kX - Stage<COLS, MT>::kZ >= 4 * MT, "row factors fit the zero-point block");
     using A = Act<kBf16>;
     using St = Stage<COLS, MT>;
     constexpr int CB = St::CB;
@@ -299,7 +310,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
         auto issue = [&](int st, int c) {
             const uint32_t base = ring + st * St::kBytes, bar = bars + 8 * st;
             const int t = (c * kChunk) >> g_shift;
-            constexpr uint32_t kBytes = kRowsPerChunk * CB * 4 + CB * 2 + (kZBulk ? CB / 2 : 0) + MT * kChunk * 2;
+            constexpr uint32_t kBytes =
+                kRowsPerChunk * CB * 4 + (kMx ? CB : CB * 2) + (kZBulk ? CB / 2 : 0) + MT * kChunk * 2;
             mbar_arrive_expect_tx(bar, kBytes);
             tma_load_2d(base + St::kQ, &a.tq, cb * CB, c * kRowsPerChunk, bar);
             tma_load_2d(base + St::kS, &a.ts, cb * CB, t, bar);
@@ -309,12 +321,37 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
 
         auto compute = [&](int st, int c) {
             const uint32_t base = ring + st * St::kBytes;
+            if constexpr (kMx) {
+                // lane l rescales x[m][l] of every row m < M; the rows' factors 2^-c go
+                // to the stage's zero-point block, unused without zero-points
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    if (m < M) {
+                        const uint32_t addr = base + St::kX + m * kChunk * 2 + lane * 2;
+                        uint16_t xb;
+                        asm volatile("ld.shared.u16 %0, [%1];" : "=h"(xb) : "r"(addr));
+                        const uint32_t emax = __reduce_max_sync(0xffffffffu, (static_cast<uint32_t>(xb) >> 7) & 0xFFu);
+                        const int sh = mx::x_shift(emax);
+                        const uint16_t xh = mx::x_to_f16(xb, sh);
+                        asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(xh) : "memory");
+                        if (lane == 0)
+                            asm volatile("st.shared.f32 [%0], %1;" ::"r"(base + St::kZ + 4 * m), "f"(mx::x_unshift(sh))
+                                         : "memory");
+                    }
+                }
+                __syncwarp();
+            }
             // scales and zero-points of the lane's columns
             uint32_t sw[G][(2 * W + 3) / 4], zw[G];
 #pragma unroll
             for (int gi = 0; gi < G; ++gi) {
                 const int c0l = St::col(lane, gi, 0);
-                lds<2 * W>(base + St::kS + c0l * 2, sw[gi]);
+                if constexpr (kMx) {
+                    uint32_t e[1];   // the W exponent bytes of the group
+                    lds<W>(base + St::kS + c0l, e);
+                    sw[gi][0] = e[0];
+                } else
+                    lds<2 * W>(base + St::kS + c0l * 2, sw[gi]);
                 if constexpr (!kSym) {
                     if constexpr (kZBulk) {
                         uint32_t v[1];
@@ -335,6 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
             };
             auto sval = [&](int j) -> float {
                 const int gi = j / W, u = j % W;
+                if constexpr (kMx) return mx::scale_f32((sw[gi][u / 4] >> (8 * (u & 3))) & 0xFFu);
                 return A::to_float(static_cast<uint16_t>(sw[gi][u / 2] >> (16 * (u & 1))));
             };
 
@@ -364,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
                     for (int j = 0; j < COLS; ++j) acc2[m][j] = 0.f;
             }
             uint32_t zz[COLS];
-            if constexpr (!kFact) {
+            if constexpr (!kFact && !kMx) {
 #pragma unroll
                 for (int j = 0; j < COLS; ++j) {
                     const uint32_t z = zval(j);
@@ -394,6 +432,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
                         h[j][1] = and_or(w, 0x00F000F0u, A::kMagic);
                         h[j][2] = and_or(w8, 0x000F000Fu, A::kMagic);
                         h[j][3] = and_or(w8, 0x00F000F0u, A::kMagic);
+                    } else if constexpr (kMx) {
+                        // (E2M1(q[k+2b]), E2M1(q[k+2b+1])) in fp16
+                        mx::e2m1x8_to_f16x2(w, h[j]);
                     } else {
 #pragma unroll
                         for (int bb = 0; bb < 4; ++bb) {
@@ -410,7 +451,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
                     if (m < M) lds<16>(base + St::kX + m * kChunk * 2 + i * 16, xw);
 #pragma unroll
                     for (int j = 0; j < COLS; ++j) {
-                        if constexpr (kTwoFamilies) {
+                        if constexpr (kMx) {
+                            // pair b holds x[k+2b], x[k+2b+1] (word b of the fp16 x row)
+#pragma unroll
+                            for (int b = 0; b < 4; ++b) {
+                                acc[m][j] = fma_mixed<false, 0, 0>(h[j][b], xw[b], acc[m][j]);
+                                acc[m][j] = fma_mixed<false, 1, 1>(h[j][b], xw[b], acc[m][j]);
+                            }
+                        } else if constexpr (kTwoFamilies) {
                             acc[m][j] = fma_mixed<false, 0, 0>(h[j][0], xw[0], acc[m][j]);
                             acc[m][j] = fma_mixed<false, 1, 0>(h[j][0], xw[2], acc[m][j]);
                             acc[m][j] = fma_mixed<false, 0, 0>(h[j][2], xw[1], acc[m][j]);
@@ -441,6 +489,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
                 for (int m = 0; m < MT; ++m) {
                     float t = acc[m][j];
                     if constexpr (kTwoFamilies) t = fmaf(acc2[m][j], 0.0625f, t);
+                    if constexpr (kMx) {
+                        if (m < M) {
+                            float u;
+                            asm volatile("ld.shared.f32 %0, [%1];" : "=f"(u) : "r"(base + St::kZ + 4 * m));
+                            t *= u;
+                        }
+                    }
                     yacc[m][j] = fmaf(s, t, yacc[m][j]);
                 }
             }
@@ -546,10 +601,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     }
 }
 
-template <bool kBf16, int MT, int COLS, bool kSym, bool kFact, bool kZBulk>
+template <bool kBf16, int MT, int COLS, bool kSym, bool kFact, bool kZBulk, bool kMx = false>
 cudaError_t launch_one(const GemvArgs& a, const GemvPlan& p, cudaStream_t s) {
     static_assert(Stage<COLS, MT>::kBytes == stage_bytes(COLS, MT), "stage layout");
-    auto kern = gemv_kernel<kBf16, MT, COLS, kSym, kFact, kZBulk>;
+    auto kern = gemv_kernel<kBf16, MT, COLS, kSym, kFact, kZBulk, kMx>;
     const size_t smem = p.smem_bytes;
     static size_t configured[64] = {0};   // largest dynamic shared memory set, per device
     const int dev = p.device;
@@ -603,6 +658,20 @@ cudaError_t launch_dtype(const GemvArgs& a, const GemvPlan& p, cudaStream_t s) {
     }
 }
 
+cudaError_t launch_mx_rows(const GemvArgs& a, const GemvPlan& p, cudaStream_t s) {
+    switch (p.mt) {
+        case 1: return launch_one<true, 1, 8, true, false, false, true>(a, p, s);
+        case 2: return launch_one<true, 2, 4, true, false, false, true>(a, p, s);
+        case 3: return launch_one<true, 3, 4, true, false, false, true>(a, p, s);
+        case 4: return launch_one<true, 4, 4, true, false, false, true>(a, p, s);
+        case 6: return launch_one<true, 6, 2, true, false, false, true>(a, p, s);
+        case 8: return launch_one<true, 8, 2, true, false, false, true>(a, p, s);
+        case 12: return launch_one<true, 12, 1, true, false, false, true>(a, p, s);
+        case 16: return launch_one<true, 16, 1, true, false, false, true>(a, p, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
 }  // namespace
 
 constexpr int kMaxLive = 512;         // max over row templates of M * columns per block
@@ -643,6 +712,21 @@ GemvPlan plan_gemv(int M, int N, int K, int g, const DeviceProps& dp) {
 
 size_t gemv_workspace_bytes(const GemvPlan& p) { return p.ticket_bytes + p.partial_bytes; }
 
+GemvPlan plan_mx_gemv(int M, int N, int K, const DeviceProps& dp) {
+    // the W4A16 plan with g = 32, minus the chunk sums of x (no zero-points):
+    // the workspace size is the same
+    GemvPlan p = plan_gemv(M, N, K, mx::kBlock, dp);
+    if (p.fact) {
+        p.fact = false;
+        const int live = p.mt * p.cb;
+        p.smem_bytes = ring_offset(live, 0) + 128 + static_cast<size_t>(kWarps) * kStages * stage_bytes(p.cols, p.mt);
+        const int per_sm = p.smem_bytes * 2 <= dp.smem_optin ? 2 : 1;
+        const long long want = static_cast<long long>(per_sm) * dp.sms;
+        p.grid = static_cast<int>(std::max<long long>(1, std::min<long long>(want, p.items / kWarps)));
+    }
+    return p;
+}
+
 cudaError_t launch_gemv(const void* x, const uint32_t* qw, const void* sc, const uint32_t* qz, void* y, int M,
                         int N, int K, int g, bool bf16, const GemvPlan& plan, void* workspace, cudaStream_t s) {
     GemvArgs a;
@@ -674,6 +758,33 @@ cudaError_t launch_gemv(const void* x, const uint32_t* qw, const void* sc, const
     a.chunks = K / kChunk;
     a.items = plan.items;
     return bf16 ? launch_dtype<true>(a, plan, s) : launch_dtype<false>(a, plan, s);
+}
+
+cudaError_t launch_mx_gemv(const void* x, const uint32_t* qw, const uint8_t* es, void* y, int M, int N, int K,
+                           const GemvPlan& plan, void* workspace, cudaStream_t s) {
+    if (plan.fact) return cudaErrorInvalidValue;   // the plan must come from plan_mx_gemv
+    GemvArgs a;
+    const uint32_t cb = static_cast<uint32_t>(plan.cb);
+    if (!encode_2d(&a.tq, CU_TENSOR_MAP_DATA_TYPE_INT32, qw, (uint64_t)N, (uint64_t)(K / 8), (uint64_t)N * 4, cb,
+                   kRowsPerChunk, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_2d(&a.ts, CU_TENSOR_MAP_DATA_TYPE_UINT8, es, (uint64_t)N, (uint64_t)(K / mx::kBlock), (uint64_t)N,
+                   cb, 1, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_2d(&a.tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, kChunk,
+                   plan.mt, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    memset(&a.tz, 0, sizeof(a.tz));
+    a.x = static_cast<const uint16_t*>(x);
+    a.qz = nullptr;
+    a.y = static_cast<uint16_t*>(y);
+    a.partials = static_cast<float*>(workspace);
+    a.tickets = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(workspace) + plan.partial_bytes);
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.g_shift = __builtin_ctz(static_cast<unsigned>(mx::kBlock));
+    a.chunks = K / kChunk;
+    a.items = plan.items;
+    return launch_mx_rows(a, plan, s);
 }
 
 // ---------------------------------------------------------------------------

@@ -38,6 +38,9 @@ struct GemvPlan {
 };
 
 GemvPlan plan_gemv(int M, int N, int K, int g, const DeviceProps& dp);
+// The GEMV plan for MXFP4 weights (no zero-points); same workspace size as
+// plan_gemv(M, N, K, 32, dp).
+GemvPlan plan_mx_gemv(int M, int N, int K, const DeviceProps& dp);
 size_t gemv_workspace_bytes(const GemvPlan& plan);
 
 // `workspace` holds plan.partial_bytes of partial-sum slots (a size fixed per
@@ -75,5 +78,15 @@ cudaError_t launch_gemm_skinny(const void* x, const uint32_t* qw, const void* sc
 cudaError_t read_and_clear_skinny_error(uint32_t* out);
 cudaError_t launch_dequant(const uint32_t* qw, const void* sc, const uint32_t* qz, void* out, int N, int K, int g,
                            bool bf16, const DeviceProps& dp, cudaStream_t s);
+
+// MXFP4 weights (E2M1 codes, E8M0 bytes [K/32, N]); bf16 activations and outputs.
+cudaError_t launch_mx_dequant(const uint32_t* qw, const uint8_t* es, void* out, int N, int K, const DeviceProps& dp,
+                              cudaStream_t s);
+cudaError_t launch_mx_gemm(const void* x, const uint32_t* qw, const uint8_t* es, void* y, int M, int N, int K,
+                           const DeviceProps& dp, cudaStream_t s);
+cudaError_t launch_mx_gemm_skinny(const void* x, const uint32_t* qw, const uint8_t* es, void* y, int M, int N, int K,
+                                  const DeviceProps& dp, cudaStream_t s);
+cudaError_t launch_mx_gemv(const void* x, const uint32_t* qw, const uint8_t* es, void* y, int M, int N, int K,
+                           const GemvPlan& plan, void* workspace, cudaStream_t s);
 
 }  // namespace w4a16

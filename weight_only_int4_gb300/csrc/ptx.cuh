@@ -104,6 +104,10 @@ __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint3
 __device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src, uint32_t src_bytes) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
+// Copy `src_bytes` (0 or 8) of the 8 bytes at src to dst; the rest is zero-filled.
+__device__ __forceinline__ void cp_async_8(uint32_t dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
 // Arrive on `bar` once every cp.async issued so far by this thread has landed. The
 // pending count is raised first, so the barrier's expected arrival count is unchanged.
 __device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
