@@ -91,6 +91,15 @@ def test_gemm_signed_scales(act):
     parity("gemm", 384, 776, 1024, 32, act, False, scales="signed", seed=5)
 
 
+@pytest.mark.parametrize("act", ["f16", "bf16"])
+@pytest.mark.parametrize("op,M", [("gemv", 1), ("gemv", 4), ("gemv", 16), ("gemm", 64), ("gemm", 384)])
+def test_q4_0_arithmetic(act, op, M):
+    """q4_0 weights ("qsa_prompt_attn: Q4_0 KV on tensor cores", section What):
+    blocks of 32, w = (code - 8) * d with a scale d of either sign -- the
+    symmetric layer at g = 32 with signed scales."""
+    parity(op, M, 776, 1024, 32, act, True, scales="signed", seed=40 + M)
+
+
 def test_gemm_k_tail_half_step():
     # K = 96 with g = 32: the last 64-deep step is half outside K
     parity("gemm", 130, 264, 96, 32, "bf16", False, seed=1)
