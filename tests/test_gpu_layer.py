@@ -53,6 +53,16 @@ def test_gemv_other_groups(g, M):
 
 
 @pytest.mark.parametrize("act", ["f16", "bf16"])
+@pytest.mark.parametrize("M", [1, 2, 3, 4])
+def test_gemv_precomputed_chunk_sums(act, M):
+    """Shapes with at least 8 chunks per warp take the GEMV variant whose chunk
+    sums of x are computed once per CTA (8192 columns, 640 chunks of K: 20480
+    column-block x chunk items for M = 1, 40960 for M = 2..4, against 8 x 16
+    warps x 152 or 304 CTAs); smaller shapes form them in each chunk."""
+    parity("gemv", M, 8192, 20480, 32, act, False, seed=90 + M)
+
+
+@pytest.mark.parametrize("act", ["f16", "bf16"])
 @pytest.mark.parametrize("M", [1, 4])
 def test_gemv_signed_scales(act, M):
     parity("gemv", M, 776, 1024, 32, act, False, scales="signed", seed=3)

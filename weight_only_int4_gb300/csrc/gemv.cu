@@ -25,7 +25,10 @@
 //     the mantissa of 1024.0 (fp16) or 128.0 (bf16). For M <= 4 the zero-point
 //     is applied once per chunk through
 //         sum_k (q - z) x = sum_k (magic + q) x - (magic + z) sum_k x,
-//     with sum_k x of every chunk precomputed in shared memory; the products
+//     with sum_k x of the chunk formed by a warp reduction over the chunk's x
+//     slice (one value per lane) when the chunk is converted, or, when every
+//     warp has many chunks to amortise it over, computed for all chunks once
+//     per CTA after the dependency wait (kXPre); the products
 //     (magic + q) * x are exact in an FP32 FMA with 16-bit inputs
 //     (fma.rn.f32.f16 / .bf16). For M > 4 the zero-point is subtracted from
 //     each nibble pair in packed 16-bit arithmetic (exact) before the FMA. The
@@ -71,7 +74,8 @@ constexpr int kL2Prefetch = W4A16_GEMV_L2_PREFETCH;
 constexpr int kThreads = kWarps * 32;
 constexpr int kChunk = 32;            // rows of K per chunk
 constexpr int kRowsPerChunk = 4;      // packed word rows per chunk
-constexpr int kFactMaxM = 4;          // zero-point by chunk sums up to this M
+constexpr int kFactMaxM = 4;          // zero-point through the chunk's sum of x up to this M
+constexpr int kXPreMinChunksPerWarp = 8;
 constexpr size_t kXsumSmemLimit = 32 * 1024;
 constexpr unsigned long long kWaitLimitCycles = 4000000000ull;   // ~2 s at 2 GHz
 constexpr unsigned int kErrTimeout = 9u;
@@ -191,7 +195,7 @@ __device__ __forceinline__ bool elect_one() {
     return pred != 0;
 }
 
-// Byte offsets inside dynamic shared memory: warp partials | chunk sums of x | barriers | rings.
+// Byte offsets inside dynamic shared memory: warp partials | chunk sums of x (kXPre) | barriers | rings.
 __host__ __device__ constexpr uint32_t xsum_offset(int live_per_warp) { return kWarps * live_per_warp * 4; }
 __host__ __device__ constexpr uint32_t bar_offset(int live_per_warp, int xsum_entries) {
     return (xsum_offset(live_per_warp) + xsum_entries * 8 + 15) & ~15u;
@@ -212,8 +216,12 @@ __device__ __forceinline__ long long range_start(int b, long long T, int G) { re
 // codes become fp16 pairs in one conversion instruction each, the products
 // are exact in an FP32 FMA with fp16 inputs, and the power of two and the
 // block scale 2^(e - 127) are applied in FP32 once per chunk.
-template <bool kBf16, int MT, int COLS, bool kSym, bool kFact, bool kZBulk, bool kMx = false>
+// kXPre (with kFact): the chunk sums of x are computed for every chunk once per
+// CTA, right after the dependency wait, instead of by a warp reduction in each
+// chunk; worth it when every warp has many chunks to amortise it over.
+template <bool kBf16, int MT, int COLS, bool kSym, bool kFact, bool kZBulk, bool kMx = false, bool kXPre = false>
 __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant__ GemvArgs a) {
+    static_assert(!kXPre || kFact, "precomputed chunk sums serve the zero-point factorisation");
     static_assert(!kMx || (kBf16 && kSym && !kFact && !kZBulk), "MXFP4: bf16, no zero-points");
     static_assert(!kMx || Stage<COLS, MT>::kX - Stage<COLS, MT>::kZ >= 4 * MT, "row factors fit the zero-point block");
     using A = Act<kBf16>;
@@ -231,9 +239,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     const long long T = a.items;
     const int Gd = gridDim.x, b = blockIdx.x;
     const long long i_begin = range_start(b, T, Gd), i_end = range_start(b + 1, T, Gd);
-    const int xs_entries = kFact ? M * chunks : 0;
     float* red = reinterpret_cast<float*>(smem);                                   // [kWarps][E]
-    float2* xsum = reinterpret_cast<float2*>(smem + xsum_offset(E));               // [M][chunks]
+    const int xs_entries = kXPre ? M * chunks : 0;
+    float2* xsum = reinterpret_cast<float2*>(smem + xsum_offset(E));               // [M][chunks] (kXPre)
     const uint32_t bars = smem_u32(smem) + bar_offset(E, xs_entries) + warp * kStages * 8;
     // rings start on a 128-byte boundary of the shared window (128 bytes of slack are reserved)
     const uint32_t ring = ((smem_u32(smem) + ring_offset(E, xs_entries) + 127u) & ~127u) + warp * kStages * St::kBytes;
@@ -267,8 +275,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     __syncthreads();
     griddep_wait();
 
-    // per (row, chunk): sum of x over the chunk and the offset the magic bias
-    // adds; computed once, while the first copies are in flight
+    // kXPre: per (row, chunk), the sum of x over the chunk and the offset the
+    // magic bias adds, computed once while the first copies are in flight
     auto chunk_sums = [&]() {
         for (int p = threadIdx.x; p < M * chunks; p += kThreads) {
             const int m = p / chunks, c = p - m * chunks;
@@ -288,11 +296,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
             xsum[p] = make_float2(off, se + so);
         }
     };
+    bool sums_pending = kXPre;
 
     uint32_t phase_bits = 0;   // parity of the next completion of each stage's barrier
     bool ok = true;
     int drain_lo = 0, drain_hi = 0;   // after a timeout: this warp's chunks whose copies may be in flight
-    bool sums_pending = kFact;
 
     for (long long it = i_begin; it < i_end;) {
         const int cb = static_cast<int>(it / chunks);
@@ -324,16 +332,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
             if constexpr (kMx) {
                 // lane l rescales x[m][l] of every row m < M; the rows' factors 2^-c go
                 // to the stage's zero-point block, unused without zero-points
+                uint16_t xb[MT];
 #pragma unroll
                 for (int m = 0; m < MT; ++m) {
+                    xb[m] = 0;
+                    if (m < M)
+                        asm volatile("ld.shared.u16 %0, [%1];" : "=h"(xb[m]) : "r"(base + St::kX + m * kChunk * 2 + lane * 2));
+                }
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    const uint32_t emax = __reduce_max_sync(0xffffffffu, (static_cast<uint32_t>(xb[m]) >> 7) & 0xFFu);
                     if (m < M) {
-                        const uint32_t addr = base + St::kX + m * kChunk * 2 + lane * 2;
-                        uint16_t xb;
-                        asm volatile("ld.shared.u16 %0, [%1];" : "=h"(xb) : "r"(addr));
-                        const uint32_t emax = __reduce_max_sync(0xffffffffu, (static_cast<uint32_t>(xb) >> 7) & 0xFFu);
                         const int sh = mx::x_shift(emax);
-                        const uint16_t xh = mx::x_to_f16(xb, sh);
-                        asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(xh) : "memory");
+                        const uint32_t addr = base + St::kX + m * kChunk * 2 + lane * 2;
+                        asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(mx::x_to_f16(xb[m], sh)) : "memory");
                         if (lane == 0)
                             asm volatile("st.shared.f32 [%0], %1;" ::"r"(base + St::kZ + 4 * m), "f"(mx::x_unshift(sh))
                                          : "memory");
@@ -376,25 +388,48 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
                 return A::to_float(static_cast<uint16_t>(sw[gi][u / 2] >> (16 * (u & 1))));
             };
 
-            // kFact: start each accumulator at -((magic + z) * sum x), so that after the
-            // chunk it holds sum (q - z) x; otherwise at 0 (z is subtracted per nibble)
+            // kFact: the accumulators collect sum (magic + q) x; (magic + z) * sum x is
+            // subtracted when the chunk is scaled, so the reduction that forms sum x
+            // runs beside the FMAs instead of ahead of them (with kXPre it is the
+            // accumulators' starting value)
             float acc[MT][COLS], acc2[kTwoFamilies ? MT : 1][kTwoFamilies ? COLS : 1];
-            if constexpr (kFact) {
-                float2 os[MT];
+            float2 os[kFact ? MT : 1];
+            if constexpr (kXPre) {
 #pragma unroll
                 for (int m = 0; m < MT; ++m) os[m] = (m < M) ? xsum[m * chunks + c] : make_float2(0.f, 0.f);
+            } else if constexpr (kFact) {
+                // per row: sum of x over the chunk and the offset the magic bias adds,
+                // from the stage's x slice (lane l holds x[m][l]; the butterfly leaves
+                // the same sums in every lane)
+                float v[MT];
 #pragma unroll
-                for (int j = 0; j < COLS; ++j) {
-                    const float zf = static_cast<float>(zval(j));
-#pragma unroll
-                    for (int m = 0; m < MT; ++m) acc[m][j] = -fmaf(zf, os[m].y, os[m].x);
+                for (int m = 0; m < MT; ++m) {
+                    uint16_t xb = 0;
+                    if (m < M)
+                        asm volatile("ld.shared.u16 %0, [%1];" : "=h"(xb) : "r"(base + St::kX + m * kChunk * 2 + lane * 2));
+                    v[m] = A::to_float(xb);
                 }
-            } else {
+                // the rows' butterflies interleaved, so their shuffle latencies overlap
 #pragma unroll
-                for (int m = 0; m < MT; ++m)
+                for (int k = 16; k >= 2; k >>= 1)
 #pragma unroll
-                    for (int j = 0; j < COLS; ++j) acc[m][j] = 0.f;
+                    for (int m = 0; m < MT; ++m) v[m] += __shfl_xor_sync(0xffffffffu, v[m], k);
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    // even lanes: sum of the low halves of x's words, odd lanes: of the high halves
+                    const float other = __shfl_xor_sync(0xffffffffu, v[m], 1);
+                    const float se = (lane & 1) ? other : v[m], so = (lane & 1) ? v[m] : other;
+                    const float off = kTwoFamilies ? fmaf(A::kMagicF, se, (A::kMagicF / 16.f) * so)
+                                                   : A::kMagicF * (se + so);
+                    os[m] = make_float2(off, se + so);
+                }
             }
+            // precomputed sums are ready at once: start at -((magic + z) * sum x)
+#pragma unroll
+            for (int m = 0; m < MT; ++m)
+#pragma unroll
+                for (int j = 0; j < COLS; ++j)
+                    acc[m][j] = kXPre ? -fmaf(static_cast<float>(zval(j)), os[m].y, os[m].x) : 0.f;
             if constexpr (kTwoFamilies) {
 #pragma unroll
                 for (int m = 0; m < MT; ++m)
@@ -489,6 +524,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
                 for (int m = 0; m < MT; ++m) {
                     float t = acc[m][j];
                     if constexpr (kTwoFamilies) t = fmaf(acc2[m][j], 0.0625f, t);
+                    if constexpr (kFact && !kXPre) t -= fmaf(static_cast<float>(zval(j)), os[m].y, os[m].x);
                     if constexpr (kMx) {
                         if (m < M) {
                             float u;
@@ -505,7 +541,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
         if (elect_one())
             for (int j = 0; j < kStages && j < nj; ++j) issue(j, c0 + warp + kWarps * j);
         __syncwarp();
-        if constexpr (kFact) {
+        if constexpr (kXPre) {
             if (sums_pending) {   // CTA-uniform: every thread runs the same segments
                 chunk_sums();
                 __syncthreads();
@@ -601,10 +637,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     }
 }
 
-template <bool kBf16, int MT, int COLS, bool kSym, bool kFact, bool kZBulk, bool kMx = false>
+template <bool kBf16, int MT, int COLS, bool kSym, bool kFact, bool kZBulk, bool kMx = false, bool kXPre = false>
 cudaError_t launch_one(const GemvArgs& a, const GemvPlan& p, cudaStream_t s) {
     static_assert(Stage<COLS, MT>::kBytes == stage_bytes(COLS, MT), "stage layout");
-    auto kern = gemv_kernel<kBf16, MT, COLS, kSym, kFact, kZBulk, kMx>;
+    auto kern = gemv_kernel<kBf16, MT, COLS, kSym, kFact, kZBulk, kMx, kXPre>;
     const size_t smem = p.smem_bytes;
     static size_t configured[64] = {0};   // largest dynamic shared memory set, per device
     const int dev = p.device;
@@ -626,16 +662,25 @@ cudaError_t launch_one(const GemvArgs& a, const GemvPlan& p, cudaStream_t s) {
     return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
-template <bool kBf16, int MT, int COLS, bool kFact>
+template <bool kBf16, int MT, int COLS, bool kFact, bool kXPre = false>
 cudaError_t launch_sym(const GemvArgs& a, const GemvPlan& p, cudaStream_t s) {
     const bool zb = (a.N % 32) == 0;
-    if (!a.qz) return launch_one<kBf16, MT, COLS, true, kFact, false>(a, p, s);
-    return zb ? launch_one<kBf16, MT, COLS, false, kFact, true>(a, p, s)
-              : launch_one<kBf16, MT, COLS, false, kFact, false>(a, p, s);
+    if (!a.qz) return launch_one<kBf16, MT, COLS, true, kFact, false, false, kXPre>(a, p, s);
+    return zb ? launch_one<kBf16, MT, COLS, false, kFact, true, false, kXPre>(a, p, s)
+              : launch_one<kBf16, MT, COLS, false, kFact, false, false, kXPre>(a, p, s);
 }
 
 template <bool kBf16>
 cudaError_t launch_dtype(const GemvArgs& a, const GemvPlan& p, cudaStream_t s) {
+    if (p.fact && p.xpre) {
+        switch (p.mt) {
+            case 1: return launch_sym<kBf16, 1, 8, true, true>(a, p, s);
+            case 2: return launch_sym<kBf16, 2, 4, true, true>(a, p, s);
+            case 3: return launch_sym<kBf16, 3, 4, true, true>(a, p, s);
+            case 4: return launch_sym<kBf16, 4, 4, true, true>(a, p, s);
+            default: break;
+        }
+    }
     if (p.fact) {
         switch (p.mt) {
             case 1: return launch_sym<kBf16, 1, 8, true>(a, p, s);
@@ -680,8 +725,11 @@ size_t partial_region_bytes(const DeviceProps& dp) {
     return static_cast<size_t>(2) * dp.sms * 2 * kMaxLive * sizeof(float);
 }
 
-GemvPlan plan_gemv(int M, int N, int K, int g, const DeviceProps& dp) {
-    (void)g;
+namespace {
+
+// `fact`: whether the kernel may apply zero-points through chunk sums of x
+// (the W4A16 layer for M <= 4; never for MXFP4 weights, which have none).
+GemvPlan plan(int M, int N, int K, bool fact, const DeviceProps& dp) {
     GemvPlan p;
     p.mt = M <= 1 ? 1 : M <= 2 ? 2 : M <= 3 ? 3 : M <= 4 ? 4 : M <= 6 ? 6 : M <= 8 ? 8 : M <= 12 ? 12 : 16;
     p.cols = p.mt == 1 ? 8 : p.mt <= 4 ? 4 : p.mt <= 8 ? 2 : 1;
@@ -691,15 +739,25 @@ GemvPlan plan_gemv(int M, int N, int K, int g, const DeviceProps& dp) {
     const int chunks = K / kChunk;
     const long long items = static_cast<long long>(p.n_cb) * chunks;
     p.items = items;
-    const size_t xsum_bytes = static_cast<size_t>(M) * chunks * sizeof(float2);
-    p.fact = M <= kFactMaxM && xsum_bytes <= kXsumSmemLimit;
+    p.fact = fact && M <= kFactMaxM;
     const int live = p.mt * p.cb;
-    p.smem_bytes = ring_offset(live, p.fact ? M * chunks : 0) + 128 +
-                   static_cast<size_t>(kWarps) * kStages * stage_bytes(p.cols, p.mt);
-    // as many CTAs per SM as shared memory allows (at most 2), each with at least one chunk per warp
-    const int per_sm = p.smem_bytes * 2 <= dp.smem_optin ? 2 : 1;
-    const long long want = static_cast<long long>(per_sm) * dp.sms;
-    p.grid = static_cast<int>(std::max<long long>(1, std::min<long long>(want, items / kWarps)));
+    auto size_grid = [&](int xsum_entries) {
+        p.smem_bytes = ring_offset(live, xsum_entries) + 128 +
+                       static_cast<size_t>(kWarps) * kStages * stage_bytes(p.cols, p.mt);
+        // as many CTAs per SM as shared memory allows (at most 2), each with at least one chunk per warp
+        const int per_sm = p.smem_bytes * 2 <= dp.smem_optin ? 2 : 1;
+        const long long want = static_cast<long long>(per_sm) * dp.sms;
+        p.grid = static_cast<int>(std::max<long long>(1, std::min<long long>(want, items / kWarps)));
+    };
+    size_grid(0);
+    // Precomputed chunk sums: a prologue over all chunks, against a warp
+    // reduction per chunk. Measured at N = 43008, K = 5376 (12 chunks per warp)
+    // the prologue wins by 0.3 us; at 4-6 chunks per warp and below the
+    // per-chunk reduction wins by 3-11 %.
+    const size_t xsum_bytes = static_cast<size_t>(M) * chunks * sizeof(float2);
+    p.xpre = p.fact && items >= static_cast<long long>(kXPreMinChunksPerWarp) * kWarps * p.grid &&
+             xsum_bytes <= kXsumSmemLimit;
+    if (p.xpre) size_grid(M * chunks);
     p.ticket_bytes = (static_cast<size_t>(p.n_cb) * sizeof(uint32_t) + 255) & ~size_t(255);
     // Partial slots first, in a region whose size depends only on the device
     // (M * columns-per-block <= kMaxLive for every row template), tickets after
@@ -710,22 +768,16 @@ GemvPlan plan_gemv(int M, int N, int K, int g, const DeviceProps& dp) {
     return p;
 }
 
+}  // namespace
+
+GemvPlan plan_gemv(int M, int N, int K, int g, const DeviceProps& dp) {
+    (void)g;
+    return plan(M, N, K, true, dp);
+}
+
 size_t gemv_workspace_bytes(const GemvPlan& p) { return p.ticket_bytes + p.partial_bytes; }
 
-GemvPlan plan_mx_gemv(int M, int N, int K, const DeviceProps& dp) {
-    // the W4A16 plan with g = 32, minus the chunk sums of x (no zero-points):
-    // the workspace size is the same
-    GemvPlan p = plan_gemv(M, N, K, mx::kBlock, dp);
-    if (p.fact) {
-        p.fact = false;
-        const int live = p.mt * p.cb;
-        p.smem_bytes = ring_offset(live, 0) + 128 + static_cast<size_t>(kWarps) * kStages * stage_bytes(p.cols, p.mt);
-        const int per_sm = p.smem_bytes * 2 <= dp.smem_optin ? 2 : 1;
-        const long long want = static_cast<long long>(per_sm) * dp.sms;
-        p.grid = static_cast<int>(std::max<long long>(1, std::min<long long>(want, p.items / kWarps)));
-    }
-    return p;
-}
+GemvPlan plan_mx_gemv(int M, int N, int K, const DeviceProps& dp) { return plan(M, N, K, false, dp); }
 
 cudaError_t launch_gemv(const void* x, const uint32_t* qw, const void* sc, const uint32_t* qz, void* y, int M,
                         int N, int K, int g, bool bf16, const GemvPlan& plan, void* workspace, cudaStream_t s) {

@@ -31,6 +31,7 @@ struct GemvPlan {
     int grid = 0;           // persistent CTAs (two per SM at most)
     long long items = 0;    // column blocks x 32-row chunks of K
     bool fact = false;      // zero-point applied per chunk through chunk sums of x
+    bool xpre = false;      // with fact: the chunk sums computed once per CTA up front
     size_t smem_bytes = 0;  // dynamic shared memory per CTA
     size_t ticket_bytes = 0;
     size_t partial_bytes = 0;
