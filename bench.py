@@ -196,8 +196,9 @@ class MxLayer:
             self.flops = 0
             return
         self.y = [torch.empty((wl.M, wl.N), dtype=torch.bfloat16, device="cuda") for _ in range(copies)]
-        if wl.kernel == "gemv":
-            self.ws = w4.new_workspace(w4.workspace_bytes(w4.OP_GEMV, wl.M, wl.N, wl.K, 32))
+        op = w4.OP_GEMV if wl.kernel == "gemv" else w4.OP_GEMM
+        nws = w4.workspace_bytes(op, wl.M, wl.N, wl.K, 32)
+        self.ws = w4.new_workspace(nws) if nws else None
         self.bytes = mx_layer_bytes(wl.M, wl.N, wl.K)
         self.flops = layer_flops(wl.M, wl.N, wl.K)
 
@@ -206,10 +207,8 @@ class MxLayer:
         for (qw, e), y in zip(self.weights, self.y):
             if self.wl.kernel == "dequant":
                 self.fn(qw, e, out=y)
-            elif self.wl.kernel == "gemv":
-                self.fn(x, qw, e, out=y, workspace=self.ws)
             else:
-                self.fn(x, qw, e, out=y)
+                self.fn(x, qw, e, out=y, workspace=self.ws)
 
 
 def time_graph(layer, steps, warmup, torch, barrier):

@@ -112,11 +112,13 @@ w4a16_status w4a16_unpack(const int32_t* src, uint8_t* dst, int64_t rows, int64_
 
 /*
  * w4a16_workspace_bytes -- bytes of device workspace `op` needs for this shape
- * on the current device; 0 for the GEMM. For the GEMV: a region of FP32
- * partial-sum slots whose size depends only on the device (16 KB per SM),
- * followed by one 32-bit ticket per column block of the shape (rounded up to
- * 256 bytes). Returns 0 for shapes the op rejects and when no GB300 is
- * current.
+ * on the current device. For the GEMV: a region of FP32 partial-sum slots
+ * whose size depends only on the device (16 KB per SM), followed by one 32-bit
+ * ticket per column block of the shape (rounded up to 256 bytes). For the GEMM
+ * with M <= 128: FP32 partial slots of 128 KB per SM, followed by four 32-bit
+ * tickets per 128 columns (rounded up to 256 bytes); 0 for the GEMM with
+ * M > 128. The same sizes serve w4a16_mxfp4_gemv and w4a16_mxfp4_gemm with
+ * g = 32. Returns 0 for shapes the op rejects and when no GB300 is current.
  */
 size_t w4a16_workspace_bytes(w4a16_op op, int64_t M, int64_t N, int64_t K, int64_t g);
 
@@ -152,7 +154,10 @@ size_t w4a16_workspace_bytes(w4a16_op op, int64_t M, int64_t N, int64_t K, int64
  *          writes partial sums only below the ticket region, so one
  *          workspace sized for the largest N serves any later call of any
  *          shape. Two calls that may run at the same time (different
- *          streams) must not share a workspace.
+ *          streams) must not share a workspace, and the GEMV and the GEMM
+ *          must not share one: the GEMM's partial-sum region covers the
+ *          GEMV's ticket words (the MXFP4 GEMV and GEMM use the same layouts
+ *          as these two and may share with them respectively).
  * Errors: NULL, SHAPE (M outside 1..16, N % 8, K % g), UNSUPPORTED (g not in
  * {32, 64, 128, 256}), DTYPE, ALIGN, WORKSPACE (NULL, unaligned or too small),
  * DEVICE, CUDA.
@@ -198,10 +203,17 @@ w4a16_status w4a16_gemv_noalloc(const void* x, const int32_t* qweight, const voi
 /*
  * w4a16_gemm -- prefill path, any M >= 1.
  *
- * M <= 128 runs an operand-swapped kernel: one CTA per 128 weight columns,
- * the dequantised weight tile as the MMA's 128-row operand and x (padded to
- * 32, 64 or 128 rows) as the other, so no MMA work is spent on 256-row tiles.
- * Larger M runs the kernel described next.
+ * M <= 128 runs an operand-swapped kernel: 128 weight columns per tile, the
+ * dequantised weight tile as the MMA's 128-row operand and x (padded to 32,
+ * 64 or 128 rows) as the other, so no MMA work is spent on 256-row tiles. Its
+ * (column block, 64-deep K step) pairs are split into equal contiguous ranges,
+ * one per SM (stream-K); a column block split between CTAs is finished by the
+ * last of them, which sums their FP32 partials from the workspace in
+ * ascending CTA order (deterministic). This path needs a workspace of
+ * w4a16_workspace_bytes(W4A16_OP_GEMM, M, N, K, g) bytes with the GEMV's
+ * ownership and zero-fill rules (W4A16_ERR_WORKSPACE otherwise); after a
+ * W4A16_ERR_TIMEOUT reported by w4a16_device_status, zero it again.
+ * Larger M runs the kernel described next and needs no workspace.
  *
  * Clusters of two CTAs (one per SM) own 256 x 256 output tiles of a
  * persistent grid. Per 64-deep K step each CTA brings its 128 rows of x and
@@ -288,12 +300,15 @@ w4a16_status w4a16_mxfp4_gemv(const void* x, const int32_t* qweight, const uint8
 
 /*
  * w4a16_mxfp4_gemm -- prefill path for MXFP4 weights, any M >= 1: the
- * w4a16_gemm kernels (operand-swapped for M <= 128, CTA pairs above) with the
- * E2M1 decode writing the bf16 operand tile. A pipeline wait that runs out
- * sets the device flag that w4a16_device_status reports.
+ * w4a16_gemm kernels (operand-swapped and stream-K for M <= 128, CTA pairs
+ * above) with the E2M1 decode writing the bf16 operand tile. Workspace as for
+ * w4a16_gemm (needed for M <= 128, sized by w4a16_workspace_bytes(
+ * W4A16_OP_GEMM, M, N, K, 32)). A pipeline wait that runs out sets the device
+ * flag that w4a16_device_status reports.
  */
 w4a16_status w4a16_mxfp4_gemm(const void* x, const int32_t* qweight, const uint8_t* escale, void* y, int64_t M,
-                              int64_t N, int64_t K, w4a16_stream stream);
+                              int64_t N, int64_t K, void* workspace, size_t workspace_bytes,
+                              w4a16_stream stream);
 
 /*
  * w4a16_device_status -- synchronise `stream`, then read and clear the

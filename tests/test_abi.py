@@ -58,7 +58,7 @@ def _gemm(lib, **kw):
     a = dict(x=P, qw=P, s=P, z=P, y=P, M=300, N=64, K=128, g=32, dt=w4.BF16)
     a.update(kw)
     return lib.w4a16_gemm(a["x"], a["qw"], a["s"], a["z"], a["y"], a["M"], a["N"], a["K"], a["g"],
-                          a["dt"], None, 0, None)
+                          a["dt"], a.get("ws", P), a.get("ws_bytes", 1 << 30), None)
 
 
 @pytest.mark.parametrize("call", [_gemv, _gemm])
@@ -129,7 +129,8 @@ def _mx(lib, fn, **kw):
     if fn == "gemv":
         return lib.w4a16_mxfp4_gemv(a["x"], a["qw"], a["e"], a["y"], a["M"], a["N"], a["K"], a.get("ws", P),
                                     a.get("ws_bytes", 1 << 30), None)
-    return lib.w4a16_mxfp4_gemm(a["x"], a["qw"], a["e"], a["y"], a["M"], a["N"], a["K"], None)
+    return lib.w4a16_mxfp4_gemm(a["x"], a["qw"], a["e"], a["y"], a["M"], a["N"], a["K"], a.get("ws", P),
+                                a.get("ws_bytes", 1 << 30), None)
 
 
 @pytest.mark.parametrize("fn", ["dequant", "gemv", "gemm"])
@@ -149,8 +150,17 @@ def test_mxfp4_rejections(lib, fn):
         assert _mx(lib, fn, x=MIS) == w4.ERR_ALIGN
     if fn == "gemv":
         assert _mx(lib, fn, M=17) == w4.ERR_SHAPE
-        assert _mx(lib, fn, ws=0) == w4.ERR_WORKSPACE
+    if fn != "dequant":
+        assert _mx(lib, fn, ws=0) == w4.ERR_WORKSPACE      # M <= 128: the GEMM needs its workspace too
         assert _mx(lib, fn, ws=MIS) == w4.ERR_WORKSPACE
+
+
+def test_gemm_few_rows_needs_a_workspace(lib):
+    # M <= 128 runs the stream-K kernel, whose partial sums live in the workspace
+    assert _gemm(lib, M=64, ws=0) == w4.ERR_WORKSPACE
+    assert _gemm(lib, M=64, ws=MIS) == w4.ERR_WORKSPACE
+    assert _gemm(lib, M=300, ws=0) == w4.ERR_DEVICE         # the CTA-pair kernel needs none
+    assert lib.w4a16_workspace_bytes(w4.OP_GEMM, 300, 64, 128, 32) == 0
 
 
 def test_valid_arguments_stop_at_the_device_gate(lib):

@@ -173,7 +173,7 @@ def test_q_equals_z_gemv_chunk_sums(M, act):
     assert np.abs(y).max() <= 1e-3 * ref_scale
 
 
-@pytest.mark.parametrize("op,M", [("gemv", 4), ("gemm", 300)])
+@pytest.mark.parametrize("op,M", [("gemv", 4), ("gemm", 300), ("gemm", 17), ("gemm", 128)])
 def test_deterministic(op, M):
     dc = DeviceCase(make_case(M, 2056, 2048, 128, "bf16", False, seed=31))
     a = run(op, dc).clone()
@@ -187,6 +187,25 @@ def test_gemv_and_gemm_agree():
     b = torch_to_f64(w4.gemm(dc.x, dc.qw, dc.s, dc.qz, 32))
     ref = dc.reference()
     assert np.abs(a - b).max() <= 2 * 1.6e-2 * np.abs(ref).max()
+
+
+def test_gemm_stream_k_workspace_reuse():
+    """The few-row GEMM splits column blocks between CTAs and settles them
+    through workspace tickets: one zeroed workspace serves calls of different
+    shapes (every call leaves its tickets at zero), split and whole blocks both
+    match the oracle, and a shape whose every block is split (fewer K-step
+    units than SMs) too."""
+    cases = [DeviceCase(make_case(M, N, K, 32, act, False, seed=M + N))
+             for (M, N, K, act) in ((17, 43008, 512, "bf16"), (64, 4104, 2048, "f16"), (128, 1032, 4096, "bf16"),
+                                    (5, 264, 256, "f16"))]
+    need = max(w4.workspace_bytes(w4.OP_GEMM, dc.case.M, dc.case.N, dc.case.K, 32) for dc in cases)
+    ws = w4.new_workspace(need)
+    for _ in range(2):
+        for dc in cases:
+            y = w4.gemm(dc.x, dc.qw, dc.s, dc.qz, 32, workspace=ws)
+            torch.cuda.synchronize()
+            assert_within_tol(y, dc.reference(), dc.act, f"gemm {dc.case.M}x{dc.case.N}x{dc.case.K}")
+    assert w4.device_status() == w4.OK
 
 
 def test_gemv_workspace_reuse_across_shapes():

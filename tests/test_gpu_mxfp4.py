@@ -180,3 +180,30 @@ def test_mx_workload_sampled_rows(name):
     rows = sorted({0, wl.M // 2, wl.M - 1, (wl.M * 5) // 7})
     assert_close(y[rows], d.reference(rows), name)
     assert w4.device_status() == w4.OK
+
+
+@pytest.mark.parametrize("op,M", [("gemv", 1), ("gemv", 5), ("gemm", 40), ("gemm", 300)])
+def test_mx_nan_byte_and_zero_x(op, M):
+    """Degenerate inputs: an E8M0 byte 255 (NaN) makes every output of its
+    column NaN and leaves the others exact; x = 0 gives y = 0 exactly."""
+    N, K = 272, 256
+    case = make_mx_case(M, N, K, seed=77)
+    case.e[3, 17] = 255
+    case.e[0, 200] = 255
+    d = MxDevice(case)
+    fn = w4.mxfp4_gemv if op == "gemv" else w4.mxfp4_gemm
+    got = torch_to_f64(fn(d.x, d.qw, d.e))
+    torch.cuda.synchronize()
+    ref = d.reference()
+    nan_cols = [17, 200]
+    assert np.all(np.isnan(got[:, nan_cols])) and np.all(np.isnan(ref[:, nan_cols]))
+    keep = [n for n in range(N) if n not in nan_cols]
+    err = np.abs(got[:, keep] - ref[:, keep]).max()
+    assert err <= TOL["bf16"] * np.abs(ref[:, keep]).max(), err
+    zero = torch.zeros_like(d.x)
+    case.e[3, 17] = case.e[0, 200] = 120
+    d = MxDevice(case)
+    y0 = fn(zero, d.qw, d.e)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(y0.float()) == 0
+    assert w4.device_status() == w4.OK

@@ -55,7 +55,7 @@ SIGNATURES = {
     "w4a16_dequant": (_INT, [_VP, _VP, _VP, _VP, _I64, _I64, _I64, _INT, _VP]),
     "w4a16_mxfp4_dequant": (_INT, [_VP, _VP, _VP, _I64, _I64, _VP]),
     "w4a16_mxfp4_gemv": (_INT, [_VP, _VP, _VP, _VP, _I64, _I64, _I64, _VP, _SZ, _VP]),
-    "w4a16_mxfp4_gemm": (_INT, [_VP, _VP, _VP, _VP, _I64, _I64, _I64, _VP]),
+    "w4a16_mxfp4_gemm": (_INT, [_VP, _VP, _VP, _VP, _I64, _I64, _I64, _VP, _SZ, _VP]),
     "w4a16_status_string": (ctypes.c_char_p, [_INT]),
     "w4a16_abi_version": (_INT, []),
 }
@@ -177,9 +177,10 @@ def new_workspace(nbytes: int, device=None):
 _workspaces = {}
 
 
-def _cached_workspace(nbytes: int, device, stream_ptr: int):
-    """One growing workspace per (device, stream): calls on one stream never overlap."""
-    key = (device.index if device.index is not None else _torch().cuda.current_device(), stream_ptr)
+def _cached_workspace(nbytes: int, device, stream_ptr: int, op: int):
+    """One growing workspace per (device, stream, op): calls on one stream never
+    overlap, and the GEMV and the GEMM lay out their workspaces differently."""
+    key = (device.index if device.index is not None else _torch().cuda.current_device(), stream_ptr, op)
     ws = _workspaces.get(key)
     if ws is None or ws.numel() < nbytes:
         ws = new_workspace(nbytes, device)
@@ -220,8 +221,9 @@ def _layer(fn_name: str, x, qweight, scales, qzeros, group_size: int, out=None, 
     lib = load_library()
     sp = _stream_ptr(stream)
     if workspace is None:
-        need = lib.w4a16_workspace_bytes(OP_GEMV if fn_name == "w4a16_gemv" else OP_GEMM, M, N, K, group_size)
-        workspace = _cached_workspace(need, x.device, sp) if need else None
+        op = OP_GEMV if fn_name == "w4a16_gemv" else OP_GEMM
+        need = lib.w4a16_workspace_bytes(op, M, N, K, group_size)
+        workspace = _cached_workspace(need, x.device, sp, op) if need else None
     ws_ptr, ws_bytes = (0, 0) if workspace is None else (workspace.data_ptr(),
                                                           workspace.numel() * workspace.element_size())
     _check(fn_name, getattr(lib, fn_name)(x.data_ptr(), qweight.data_ptr(), scales.data_ptr(), zp,
@@ -305,15 +307,16 @@ def _mx_layer(fn_name: str, x, qweight, escale, out, workspace, stream):
         raise ValueError(f"out must be bf16 [M, N] = [{M}, {N}]")
     lib = load_library()
     sp = _stream_ptr(stream)
-    if fn_name == "w4a16_mxfp4_gemm":
-        _check(fn_name, lib.w4a16_mxfp4_gemm(x.data_ptr(), qweight.data_ptr(), escale.data_ptr(), out.data_ptr(),
-                                              M, N, K, sp))
-        return out
     if workspace is None:
-        need = lib.w4a16_workspace_bytes(OP_GEMV, M, N, K, 32)
-        workspace = _cached_workspace(need, x.device, sp) if need else None
+        op = OP_GEMM if fn_name == "w4a16_mxfp4_gemm" else OP_GEMV
+        need = lib.w4a16_workspace_bytes(op, M, N, K, 32)
+        workspace = _cached_workspace(need, x.device, sp, op) if need else None
     ws_ptr, ws_bytes = (0, 0) if workspace is None else (workspace.data_ptr(),
                                                           workspace.numel() * workspace.element_size())
+    if fn_name == "w4a16_mxfp4_gemm":
+        _check(fn_name, lib.w4a16_mxfp4_gemm(x.data_ptr(), qweight.data_ptr(), escale.data_ptr(), out.data_ptr(),
+                                              M, N, K, ws_ptr, ws_bytes, sp))
+        return out
     _check(fn_name, lib.w4a16_mxfp4_gemv(x.data_ptr(), qweight.data_ptr(), escale.data_ptr(), out.data_ptr(),
                                           M, N, K, ws_ptr, ws_bytes, sp))
     return out
@@ -325,9 +328,9 @@ def mxfp4_gemv(x, qweight, escale, out=None, workspace=None, stream=None):
     return _mx_layer("w4a16_mxfp4_gemv", x, qweight, escale, out, workspace, stream)
 
 
-def mxfp4_gemm(x, qweight, escale, out=None, stream=None):
+def mxfp4_gemm(x, qweight, escale, out=None, workspace=None, stream=None):
     """Prefill path for MXFP4 weights (any M >= 1, tcgen05). Returns bf16 y [M, N]."""
-    return _mx_layer("w4a16_mxfp4_gemm", x, qweight, escale, out, None, stream)
+    return _mx_layer("w4a16_mxfp4_gemm", x, qweight, escale, out, workspace, stream)
 
 
 def mxfp4_dequant(qweight, escale, out=None, stream=None):

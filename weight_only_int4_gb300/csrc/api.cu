@@ -144,11 +144,14 @@ w4a16_status w4a16_unpack(const int32_t* src, uint8_t* dst, int64_t rows, int64_
 }
 
 size_t w4a16_workspace_bytes(w4a16_op op, int64_t M, int64_t N, int64_t K, int64_t g) {
-    if (op != W4A16_OP_GEMV) return 0;
-    if (M < 1 || M > 16 || N < 8 || N % 8 || K < 1 || K > kMaxDim || N > kMaxDim || !supported_group(g) || K % g)
+    if (op != W4A16_OP_GEMV && op != W4A16_OP_GEMM) return 0;
+    if (M < 1 || N < 8 || N % 8 || K < 1 || K > kMaxDim || N > kMaxDim || M > kMaxDim || !supported_group(g) || K % g)
         return 0;
+    if (op == W4A16_OP_GEMV && M > 16) return 0;
+    if (op == W4A16_OP_GEMM && M > w4a16::kSkinnyMaxM) return 0;
     DeviceProps dp;
     if (device_gate(&dp) != W4A16_OK) return 0;
+    if (op == W4A16_OP_GEMM) return w4a16::skinny_workspace_bytes((int)N, dp);
     return w4a16::gemv_workspace_bytes(w4a16::plan_gemv((int)M, (int)N, (int)K, (int)g, dp));
 }
 
@@ -190,17 +193,18 @@ w4a16_status w4a16_gemv_noalloc(const void* x, const int32_t* qweight, const voi
 w4a16_status w4a16_gemm(const void* x, const int32_t* qweight, const void* scales, const int32_t* qzeros, void* y,
                         int64_t M, int64_t N, int64_t K, int64_t g, w4a16_dtype dt, void* workspace,
                         size_t workspace_bytes, w4a16_stream stream) {
-    (void)workspace;
-    (void)workspace_bytes;
     w4a16_status st = check_layer_args(x, qweight, scales, qzeros, y, M, N, K, g, dt, 0);
     if (st != W4A16_OK) return st;
+    if (M <= w4a16::kSkinnyMaxM && (!workspace || !aligned16(workspace))) return W4A16_ERR_WORKSPACE;
     DeviceProps dp;
     if ((st = device_gate(&dp)) != W4A16_OK) return st;
-    if (M <= w4a16::kSkinnyMaxM)
+    if (M <= w4a16::kSkinnyMaxM) {
+        if (workspace_bytes < w4a16::skinny_workspace_bytes((int)N, dp)) return W4A16_ERR_WORKSPACE;
         return from_cuda(w4a16::launch_gemm_skinny(x, reinterpret_cast<const uint32_t*>(qweight), scales,
                                                    reinterpret_cast<const uint32_t*>(qzeros), y, (int)M, (int)N,
-                                                   (int)K, (int)g, dt == W4A16_BF16, dp,
+                                                   (int)K, (int)g, dt == W4A16_BF16, workspace, dp,
                                                    reinterpret_cast<cudaStream_t>(stream)));
+    }
     return from_cuda(w4a16::launch_gemm(x, reinterpret_cast<const uint32_t*>(qweight), scales,
                                         reinterpret_cast<const uint32_t*>(qzeros), y, (int)M, (int)N, (int)K, (int)g,
                                         dt == W4A16_BF16, dp, reinterpret_cast<cudaStream_t>(stream)));
@@ -260,15 +264,18 @@ w4a16_status w4a16_mxfp4_gemv(const void* x, const int32_t* qweight, const uint8
 }
 
 w4a16_status w4a16_mxfp4_gemm(const void* x, const int32_t* qweight, const uint8_t* escale, void* y, int64_t M,
-                              int64_t N, int64_t K, w4a16_stream stream) {
+                              int64_t N, int64_t K, void* workspace, size_t workspace_bytes, w4a16_stream stream) {
     w4a16_status st = check_mx_args(x, qweight, escale, y, M, N, K, 0);
     if (st != W4A16_OK) return st;
+    if (M <= w4a16::kSkinnyMaxM && (!workspace || !aligned16(workspace))) return W4A16_ERR_WORKSPACE;
     DeviceProps dp;
     if ((st = device_gate(&dp)) != W4A16_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const uint32_t* qw = reinterpret_cast<const uint32_t*>(qweight);
-    if (M <= w4a16::kSkinnyMaxM)
-        return from_cuda(w4a16::launch_mx_gemm_skinny(x, qw, escale, y, (int)M, (int)N, (int)K, dp, s));
+    if (M <= w4a16::kSkinnyMaxM) {
+        if (workspace_bytes < w4a16::skinny_workspace_bytes((int)N, dp)) return W4A16_ERR_WORKSPACE;
+        return from_cuda(w4a16::launch_mx_gemm_skinny(x, qw, escale, y, (int)M, (int)N, (int)K, workspace, dp, s));
+    }
     return from_cuda(w4a16::launch_mx_gemm(x, qw, escale, y, (int)M, (int)N, (int)K, dp, s));
 }
 

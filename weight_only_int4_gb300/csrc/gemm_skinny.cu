@@ -13,7 +13,18 @@
 // section "Confirmed mechanism"), as in the prefill GEMM, but no tile is
 // padded to 256 rows of x.
 //
-// Warp roles, one CTA per SM, persistent over column blocks:
+// Work is split stream-K: the (column block, K step) pairs, column block
+// first, are cut into equal contiguous ranges, one per CTA (one CTA per SM),
+// so every SM dequantises the same number of steps whatever the number of
+// column blocks (336 blocks over 152 SMs would otherwise leave a third of the
+// SMs idle in the last round). A column block whose steps are split between
+// CTAs is finished by the last of them to arrive: each writes its FP32
+// partial [M x 128] to a workspace slot, takes the block's ticket, and the
+// last one sums the partials in ascending CTA order (deterministic) and
+// stores y.
+//
+// Warp roles, one CTA per SM, each walking the CTA's (column block, K range)
+// segments in order:
 //   warp 0      producer: per 64-deep K step, TMA brings the x tile [MP x 64]
 //               (128-byte swizzle, rows >= M zero-filled) and the packed weight
 //               tile [8 words x 128]; the lanes stage the step's scales and
@@ -118,6 +129,40 @@ __device__ __forceinline__ bool warp_wait_bar(uint32_t bar, uint32_t parity, vol
     return ok != 0;
 }
 
+// The CTA's range of (column block, K step) units, column block first, walked
+// as segments: column block t, K steps [k0, k1).
+// Without stream-K the CTA takes whole column blocks blockIdx.x, + gridDim.x, ...
+struct Segments {
+    long long u, u_end;
+    int kt_total;
+    bool streamk;
+    int tiles;
+    __device__ bool next(int& t, int& k0, int& k1) {
+        if (!streamk) {
+            if (u >= tiles) return false;
+            t = static_cast<int>(u);
+            k0 = 0;
+            k1 = kt_total;
+            u += gridDim.x;
+            return true;
+        }
+        if (u >= u_end) return false;
+        t = static_cast<int>(u / kt_total);
+        k0 = static_cast<int>(u - static_cast<long long>(t) * kt_total);
+        k1 = static_cast<int>(u_end - u < kt_total - k0 ? k0 + (u_end - u) : kt_total);
+        u += k1 - k0;
+        return true;
+    }
+};
+__device__ __forceinline__ long long unit_start(int b, long long U, int G) { return static_cast<long long>(b) * U / G; }
+// the CTA whose range holds unit u
+__device__ __forceinline__ int unit_owner(long long u, long long U, int G) { return static_cast<int>(((u + 1) * G - 1) / U); }
+#ifndef W4A16_SKINNY_STREAMK_MAX_M
+#define W4A16_SKINNY_STREAMK_MAX_M 128
+#endif
+constexpr int kStreamKMaxM = W4A16_SKINNY_STREAMK_MAX_M;   // larger M: whole column blocks per CTA
+constexpr int kSlotFloats = BN * 128;   // one partial [BN columns][up to 128 rows], rows contiguous
+
 template <bool kBf16>
 struct Dq;
 template <>
@@ -157,7 +202,7 @@ template <bool kBf16, bool kSym, int MP, bool kMx = false>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
                    const uint16_t* __restrict__ sc, const uint32_t* __restrict__ qz, uint16_t* __restrict__ y, int M,
-                   int N, int K, int g) {
+                   int N, int K, int g, float* __restrict__ partials, uint32_t* __restrict__ tickets, int streamk) {
     using C = Cfg<MP>;
     constexpr int L = C::kLoadStages;
     extern __shared__ uint8_t smem_raw[];
@@ -178,6 +223,10 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_cons
     const int kt_total = (K + BK - 1) / BK;
     const int groups = K / g;
     volatile int* abort_flag = &bars->abort;
+    const long long U = static_cast<long long>(tiles) * kt_total;
+    const int G = gridDim.x;
+    const long long u_begin = streamk ? unit_start(blockIdx.x, U, G) : blockIdx.x;
+    const long long u_end = streamk ? unit_start(blockIdx.x + 1, U, G) : tiles;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < L; ++s) {
@@ -213,10 +262,12 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_cons
         bool issued[L];
         for (int s = 0; s < L; ++s) issued[s] = false, issued_parity[s] = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+        Segments seg{u_begin, u_end, kt_total, streamk != 0, tiles};
+        int t, k0, k1;
+        while (ok && seg.next(t, k0, k1)) {
             const int n0 = t * BN;
             const int n = n0 + 8 * sub;
-            for (int kt = 0; kt < kt_total; ++kt) {
+            for (int kt = k0; kt < k1; ++kt) {
                 if (!warp_wait_bar(smem_u32(&bars->lempty[stage]), phase ^ 1u, abort_flag, lane)) { ok = false; break; }
                 const uint32_t fb = smem_u32(&bars->lfull[stage]);
                 const int grp = (kt * BK + half * (BK / 2)) / g;
@@ -263,11 +314,13 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_cons
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+            Segments seg{u_begin, u_end, kt_total, streamk != 0, tiles};
+            int t, k0, k1;
+            while (ok && seg.next(t, k0, k1)) {
                 if (!wait_bar(smem_u32(&bars->tempty[acc]), acc_phase ^ 1u, abort_flag)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * C::kAccCols);
-                for (int kt = 0; kt < kt_total; ++kt) {
+                for (int kt = k0; kt < k1; ++kt) {
                     // completes when the dequant group has written the operand tile,
                     // which it starts only after the step's x tile has landed
                     if (!wait_bar(smem_u32(&bars->bfull[bs]), bph, abort_flag)) { ok = false; break; }
@@ -276,7 +329,7 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_cons
                     const uint64_t xdesc = sw128_kmajor_desc(ld_a(ls));
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)
-                        umma_f16(d_tmem, wdesc + 2u * kk, xdesc + 2u * kk, kIdesc, (kt | kk) != 0);
+                        umma_f16(d_tmem, wdesc + 2u * kk, xdesc + 2u * kk, kIdesc, (kt - k0) + kk != 0);
                     umma_commit(smem_u32(&bars->lempty[ls]));
                     umma_commit(smem_u32(&bars->bempty[bs]));
                     if (++ls == L) ls = 0;
@@ -295,12 +348,18 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_cons
     } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 4) {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;                 // tensor-memory lane quarter: columns 32q .. 32q+31
+        const int et = threadIdx.x - kEpiWarp0 * 32;   // 0..127: column of the block
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
+        Segments seg{u_begin, u_end, kt_total, streamk != 0, tiles};
+        int t, k0, k1;
+        while (seg.next(t, k0, k1)) {
             if (!warp_wait_bar(smem_u32(&bars->tfull[acc]), acc_phase, abort_flag, lane)) break;
             tc_fence_after();
             const int n = t * BN + q * 32 + lane;
+            const bool whole = k0 == 0 && k1 == kt_total;
+            // a split block: slot 1 for the segment that starts the block, 0 for the others
+            float* part = partials + (static_cast<size_t>(blockIdx.x) * 2 + (k0 > 0 ? 0 : 1)) * kSlotFloats;
 #pragma unroll 1
             for (int ch = 0; ch < MP / 32; ++ch) {
                 uint32_t r[32];
@@ -308,18 +367,72 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_cons
                                        static_cast<uint32_t>(acc * C::kAccCols + ch * 32),
                                    r);
                 tmem_wait_ld();
-                if (n < N) {
+                if (whole) {
+                    if (n < N) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int m = ch * 32 + i;
-                        if (m < M) y[static_cast<size_t>(m) * N + n] = Dq<kBf16>::out(__uint_as_float(r[i]));
+                        for (int i = 0; i < 32; ++i) {
+                            const int m = ch * 32 + i;
+                            if (m < M) y[static_cast<size_t>(m) * N + n] = Dq<kBf16>::out(__uint_as_float(r[i]));
+                        }
                     }
+                } else if (ch * 32 < M) {
+                    // this column's rows ch*32 .. ch*32+31, contiguous (rows >= M are never read)
+                    float4* dst = reinterpret_cast<float4*>(part + et * 128 + ch * 32);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        dst[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                                             __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
                 }
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&bars->tempty[acc]));
             if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+            if (whole) continue;
+            // split block: each warp settles its 32 columns on its own (a ticket per
+            // column block and warp, no barrier across warps): the last contributing
+            // CTA to arrive sums every contributor's partial in ascending CTA order
+            // and stores y
+            const long long first = static_cast<long long>(t) * kt_total;
+            const int b_lo = unit_owner(first, U, G), b_hi = unit_owner(first + kt_total - 1, U, G);
+            __threadfence();
+            __syncwarp();
+            uint32_t last = 0;
+            if (lane == 0) last = atomicAdd(tickets + 4 * t + q, 1u) == static_cast<unsigned>(b_hi - b_lo);
+            last = __shfl_sync(0xffffffffu, last, 0);
+            if (last) {
+                __threadfence();
+                if (n < N) {
+                    // rows in batches of 16: four 16-byte loads per contributor in flight
+                    for (int m0 = 0; m0 < M; m0 += 16) {
+                        float4 acc4[4];
+                        const float4* lo =
+                            reinterpret_cast<const float4*>(partials + (static_cast<size_t>(b_lo) * 2 + 1) * kSlotFloats +
+                                                            et * 128 + m0);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) acc4[i] = __ldcg(lo + i);
+                        for (int b0 = b_lo + 1; b0 <= b_hi; ++b0) {
+                            const float4* src = reinterpret_cast<const float4*>(
+                                partials + static_cast<size_t>(b0) * 2 * kSlotFloats + et * 128 + m0);
+                            float4 v[4];
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) v[i] = __ldcg(src + i);
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                acc4[i].x += v[i].x;
+                                acc4[i].y += v[i].y;
+                                acc4[i].z += v[i].z;
+                                acc4[i].w += v[i].w;
+                            }
+                        }
+                        const float* f = reinterpret_cast<const float*>(acc4);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            if (m0 + i < M) y[static_cast<size_t>(m0 + i) * N + n] = Dq<kBf16>::out(f[i]);
+                    }
+                }
+                if (lane == 0) tickets[4 * t + q] = 0u;
+            }
         }
     } else if (warp >= kDeqWarp0) {
         // ------------------------------------------------------------ dequantisers
@@ -337,8 +450,10 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_cons
             if (++ls == L) { ls = 0; lph ^= 1u; }
             if (++bs == kBStages) { bs = 0; bph ^= 1u; }
         };
-        for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
-            for (int kt = 0; kt < kt_total; ++kt) {
+        Segments seg{u_begin, u_end, kt_total, streamk != 0, tiles};
+        int t, k0, k1;
+        while (ok && seg.next(t, k0, k1)) {
+            for (int kt = k0; kt < k1; ++kt) {
                 if (j % kDeqGroups != grp) {
                     advance();
                     continue;
@@ -403,7 +518,7 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_cons
 
 template <bool kBf16, bool kSym, int MP, bool kMx = false>
 cudaError_t launch_mp(const void* x, const uint32_t* qw, const void* sc, const uint32_t* qz, void* y, int M, int N,
-                      int K, int g, const DeviceProps& dp, cudaStream_t s) {
+                      int K, int g, void* workspace, const DeviceProps& dp, cudaStream_t s) {
     auto kern = gemm_skinny_kernel<kBf16, kSym, MP, kMx>;
     constexpr size_t kSmem = smem_bytes<MP>();
     static_assert(kSmem <= 227 * 1024, "shared memory budget");
@@ -421,37 +536,50 @@ cudaError_t launch_mp(const void* x, const uint32_t* qw, const void* sc, const u
                    BK / 8, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
     const int tiles = (N + BN - 1) / BN;
-    const int grid = std::max(1, std::min(tiles, dp.sms));
+    const long long units = static_cast<long long>(tiles) * ((K + BK - 1) / BK);
+    const bool streamk = M <= kStreamKMaxM;
+    const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(streamk ? units : tiles, dp.sms)));
+    float* partials = static_cast<float*>(workspace);
+    uint32_t* tickets = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(workspace) + skinny_partial_bytes(dp));
     kern<<<grid, kThreads, kSmem, s>>>(tx, tw, static_cast<const uint16_t*>(sc), qz, static_cast<uint16_t*>(y), M, N, K,
-                                       g);
+                                       g, partials, tickets, streamk ? 1 : 0);
     return cudaGetLastError();
 }
 
 template <bool kBf16, bool kSym, bool kMx = false>
 cudaError_t launch_typed(const void* x, const uint32_t* qw, const void* sc, const uint32_t* qz, void* y, int M, int N,
-                         int K, int g, const DeviceProps& dp, cudaStream_t s) {
-    if (M <= 32) return launch_mp<kBf16, kSym, 32, kMx>(x, qw, sc, qz, y, M, N, K, g, dp, s);
-    if (M <= 64) return launch_mp<kBf16, kSym, 64, kMx>(x, qw, sc, qz, y, M, N, K, g, dp, s);
-    if (M <= 128) return launch_mp<kBf16, kSym, 128, kMx>(x, qw, sc, qz, y, M, N, K, g, dp, s);
-    return launch_mp<kBf16, kSym, 256, kMx>(x, qw, sc, qz, y, M, N, K, g, dp, s);
+                         int K, int g, void* ws, const DeviceProps& dp, cudaStream_t s) {
+    if (M <= 32) return launch_mp<kBf16, kSym, 32, kMx>(x, qw, sc, qz, y, M, N, K, g, ws, dp, s);
+    if (M <= 64) return launch_mp<kBf16, kSym, 64, kMx>(x, qw, sc, qz, y, M, N, K, g, ws, dp, s);
+    return launch_mp<kBf16, kSym, 128, kMx>(x, qw, sc, qz, y, M, N, K, g, ws, dp, s);
 }
 
 }  // namespace
 
+size_t skinny_partial_bytes(const DeviceProps& dp) {
+    return static_cast<size_t>(dp.sms) * 2 * kSlotFloats * sizeof(float);
+}
+
+size_t skinny_workspace_bytes(int N, const DeviceProps& dp) {
+    // one ticket per column block and epilogue warp
+    const size_t tickets = (static_cast<size_t>((N + BN - 1) / BN) * 4 * sizeof(uint32_t) + 255) & ~size_t(255);
+    return skinny_partial_bytes(dp) + tickets;
+}
+
 cudaError_t launch_gemm_skinny(const void* x, const uint32_t* qw, const void* sc, const uint32_t* qz, void* y, int M,
-                               int N, int K, int g, bool bf16, const DeviceProps& dp, cudaStream_t s) {
-    if (M < 1 || M > kSkinnyMaxM) return cudaErrorInvalidValue;
+                               int N, int K, int g, bool bf16, void* ws, const DeviceProps& dp, cudaStream_t s) {
+    if (M < 1 || M > kSkinnyMaxM || M > 128 || !ws) return cudaErrorInvalidValue;
     if (bf16)
-        return qz ? launch_typed<true, false>(x, qw, sc, qz, y, M, N, K, g, dp, s)
-                  : launch_typed<true, true>(x, qw, sc, qz, y, M, N, K, g, dp, s);
-    return qz ? launch_typed<false, false>(x, qw, sc, qz, y, M, N, K, g, dp, s)
-              : launch_typed<false, true>(x, qw, sc, qz, y, M, N, K, g, dp, s);
+        return qz ? launch_typed<true, false>(x, qw, sc, qz, y, M, N, K, g, ws, dp, s)
+                  : launch_typed<true, true>(x, qw, sc, qz, y, M, N, K, g, ws, dp, s);
+    return qz ? launch_typed<false, false>(x, qw, sc, qz, y, M, N, K, g, ws, dp, s)
+              : launch_typed<false, true>(x, qw, sc, qz, y, M, N, K, g, ws, dp, s);
 }
 
 cudaError_t launch_mx_gemm_skinny(const void* x, const uint32_t* qw, const uint8_t* es, void* y, int M, int N, int K,
-                                  const DeviceProps& dp, cudaStream_t s) {
-    if (M < 1 || M > kSkinnyMaxM) return cudaErrorInvalidValue;
-    return launch_typed<true, true, true>(x, qw, es, nullptr, y, M, N, K, mx::kBlock, dp, s);
+                                  void* ws, const DeviceProps& dp, cudaStream_t s) {
+    if (M < 1 || M > kSkinnyMaxM || M > 128 || !ws) return cudaErrorInvalidValue;
+    return launch_typed<true, true, true>(x, qw, es, nullptr, y, M, N, K, mx::kBlock, ws, dp, s);
 }
 
 }  // namespace w4a16

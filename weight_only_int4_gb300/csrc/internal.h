@@ -74,8 +74,14 @@ cudaError_t launch_wait_selftest(cudaStream_t s);
 #define W4A16_SKINNY_MAX_M 128
 #endif
 constexpr int kSkinnyMaxM = W4A16_SKINNY_MAX_M;
+// The operand-swapped kernel splits its work stream-K; its workspace holds FP32
+// partial slots (two per CTA; the size depends only on the device) followed by
+// one ticket word per column block and epilogue warp (zero before the first
+// call; every call leaves them zero).
+size_t skinny_partial_bytes(const DeviceProps& dp);
+size_t skinny_workspace_bytes(int N, const DeviceProps& dp);
 cudaError_t launch_gemm_skinny(const void* x, const uint32_t* qw, const void* sc, const uint32_t* qz, void* y, int M,
-                               int N, int K, int g, bool bf16, const DeviceProps& dp, cudaStream_t s);
+                               int N, int K, int g, bool bf16, void* ws, const DeviceProps& dp, cudaStream_t s);
 cudaError_t read_and_clear_skinny_error(uint32_t* out);
 cudaError_t launch_dequant(const uint32_t* qw, const void* sc, const uint32_t* qz, void* out, int N, int K, int g,
                            bool bf16, const DeviceProps& dp, cudaStream_t s);
@@ -86,7 +92,7 @@ cudaError_t launch_mx_dequant(const uint32_t* qw, const uint8_t* es, void* out, 
 cudaError_t launch_mx_gemm(const void* x, const uint32_t* qw, const uint8_t* es, void* y, int M, int N, int K,
                            const DeviceProps& dp, cudaStream_t s);
 cudaError_t launch_mx_gemm_skinny(const void* x, const uint32_t* qw, const uint8_t* es, void* y, int M, int N, int K,
-                                  const DeviceProps& dp, cudaStream_t s);
+                                  void* ws, const DeviceProps& dp, cudaStream_t s);
 cudaError_t launch_mx_gemv(const void* x, const uint32_t* qw, const uint8_t* es, void* y, int M, int N, int K,
                            const GemvPlan& plan, void* workspace, cudaStream_t s);
 
