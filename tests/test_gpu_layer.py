@@ -116,6 +116,14 @@ def test_gemm_k_tail_half_step():
     parity("gemm", 130, 264, 160, 32, "f16", True, seed=2)
 
 
+@pytest.mark.parametrize("M", [17, 64, 100])
+@pytest.mark.parametrize("K", [96, 160, 224, 288])
+def test_gemm_few_rows_k_tail(M, K):
+    """The few-row kernel steps 128 deep for up to 64 padded rows of x (64 deep
+    above): K = 96 .. 288 leaves the last step 1/4 to 3/4 outside K."""
+    parity("gemm", M, 520, K, 32, "bf16", M % 2 == 0, seed=K + M)
+
+
 def test_gemm_many_tiles_multiple_waves():
     # more tiles than SMs: every CTA loops over several tiles and both accumulators
     parity("gemm", 1024, 8192, 256, 128, "bf16", False, seed=9)

@@ -25,15 +25,17 @@
 //
 // Warp roles, one CTA per SM, each walking the CTA's (column block, K range)
 // segments in order:
-//   warp 0      producer: per 64-deep K step, TMA brings the x tile [MP x 64]
-//               (128-byte swizzle, rows >= M zero-filled) and the packed weight
-//               tile [8 words x 128]; the lanes stage the step's scales and
-//               zero-point words with cp.async. One mbarrier per stage.
+//   warp 0      producer: per K step (128 deep for up to 64 padded rows of x,
+//               else 64), TMA brings the x tile [MP x step] in 64-column
+//               boxes (128-byte swizzle, rows >= M zero-filled) and the packed
+//               weight tile [step/8 words x 128]; the lanes stage the step's
+//               scales and zero-point words with cp.async. One mbarrier per stage.
 //   warps 8-23  two groups of eight on alternate K steps dequantise the packed
-//               tile into the canonical K-major 128-byte-swizzled operand tile:
-//               w = (q - z) * s, (q - z) exact in 16-bit arithmetic, one rounding.
-//   warp 1      one thread issues 4 x tcgen05.mma (kind::f16, M=128, N=MP,
-//               K=16) per step into one of two MP-column FP32 accumulators.
+//               tile into the canonical K-major 128-byte-swizzled operand tile
+//               (one or two 64-deep sub-tiles): w = (q - z) * s, (q - z) exact
+//               in 16-bit arithmetic, one rounding.
+//   warp 1      one thread issues step/16 x tcgen05.mma (kind::f16, M=128,
+//               N=MP, K=16) per step into one of two MP-column FP32 accumulators.
 //   warps 4-7   epilogue: tcgen05.ld of the accumulator (lane = column n,
 //               column = row m of x), round, store y[m][n] (consecutive lanes
 //               write consecutive columns), predicated on m < M and n < N.
@@ -56,17 +58,20 @@ __device__ unsigned int g_skinny_error = 0;
 
 namespace {
 
-constexpr int BN = 128, BK = 64;         // weight columns per tile (M of the MMA), K per step
+// Row buckets up to this many padded rows of x take 128-deep K steps (twice the
+// work per pipeline hand-off); larger ones 64-deep steps, which leave room for
+// more load stages. Measured at N = 43008, K = 5376: 128-deep steps 6-10 %
+// faster for M <= 64, twice as slow at MP = 128 (two load stages).
+#ifndef W4A16_SKINNY_BK128_MAX_MP
+#define W4A16_SKINNY_BK128_MAX_MP 64
+#endif
+constexpr int BN = 128;                  // weight columns per tile (M of the MMA)
 constexpr int kThreads = 768;
 constexpr int kEpiWarp0 = 4;             // warps 4..7
 constexpr int kDeqWarp0 = 8;             // warps 8..23: two groups taking alternate K steps
 constexpr int kDeqWarps = 8;
 constexpr int kDeqGroups = 2;
-constexpr int kBStages = 4;
-constexpr uint32_t kWBytes = (BK / 8) * BN * 4;      //  4 KB packed weights
-constexpr uint32_t kSBytes = 2 * BN * 2;             // scales of the two 32-row halves of a step
-constexpr uint32_t kZBytes = 2 * (BN / 8) * 4;       // zero-point words of the two halves
-constexpr uint32_t kBBytes = BN * BK * 2;            // 16 KB dequantised operand tile
+constexpr uint32_t kSubBytes = BN * 64 * 2;          // 16 KB: one 64-deep sub-tile of the operand
 constexpr uint32_t kSuspendNs = 20000;
 constexpr unsigned long long kWaitLimitCycles = 4000000000ull;   // ~2 s at 2 GHz
 constexpr unsigned int kErrTimeout = 9u;
@@ -75,6 +80,14 @@ constexpr size_t kSmemBudget = 220 * 1024;
 template <int MP>
 struct Cfg {
     static_assert(MP % 32 == 0 && MP >= 32 && MP <= 256, "rows of x per tile");
+    static constexpr int BK = MP <= W4A16_SKINNY_BK128_MAX_MP ? 128 : 64;   // K per step
+    static constexpr int kSub = BK / 64;            // 64-deep sub-tiles per step (one 128-byte swizzle row each)
+    static constexpr int kQuarters = BK / 32;       // 32-row scale blocks per step
+    static constexpr int kBStages = BK == 128 ? 2 : 4;
+    static constexpr uint32_t kWBytes = (BK / 8) * BN * 4;          // packed weights
+    static constexpr uint32_t kSBytes = kQuarters * BN * 2;         // scales of the step's 32-row blocks
+    static constexpr uint32_t kZBytes = kQuarters * (BN / 8) * 4;   // zero-point words of the blocks
+    static constexpr uint32_t kBBytes = kSub * kSubBytes;           // dequantised operand tile
     static constexpr uint32_t kABytes = MP * BK * 2;                                   // x tile
     static constexpr uint32_t kLoadStageBytes = (kABytes + kWBytes + kSBytes + kZBytes + 1023) & ~1023u;
     // as many load stages as fit beside the operand ring, an even number (each
@@ -92,8 +105,8 @@ template <int MP>
 struct __align__(8) Barriers {
     uint64_t lfull[Cfg<MP>::kLoadStages];
     uint64_t lempty[Cfg<MP>::kLoadStages];
-    uint64_t bfull[kBStages];
-    uint64_t bempty[kBStages];
+    uint64_t bfull[Cfg<MP>::kBStages];
+    uint64_t bempty[Cfg<MP>::kBStages];
     uint64_t tfull[2];
     uint64_t tempty[2];
     uint64_t drain;
@@ -103,7 +116,8 @@ struct __align__(8) Barriers {
 
 template <int MP>
 constexpr size_t smem_bytes() {
-    return 1024 + Cfg<MP>::kLoadStages * Cfg<MP>::kLoadStageBytes + kBStages * kBBytes + sizeof(Barriers<MP>);
+    return 1024 + Cfg<MP>::kLoadStages * Cfg<MP>::kLoadStageBytes + Cfg<MP>::kBStages * Cfg<MP>::kBBytes +
+           sizeof(Barriers<MP>);
 }
 
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort) {
@@ -205,6 +219,8 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_cons
                    int N, int K, int g, float* __restrict__ partials, uint32_t* __restrict__ tickets, int streamk) {
     using C = Cfg<MP>;
     constexpr int L = C::kLoadStages;
+    constexpr int BK = C::BK, kSub = C::kSub, kBStages = C::kBStages;
+    constexpr uint32_t kWBytes = C::kWBytes, kSBytes = C::kSBytes, kBBytes = C::kBBytes;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* bsmem = smem + L * C::kLoadStageBytes;
@@ -270,24 +286,30 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_cons
             for (int kt = k0; kt < k1; ++kt) {
                 if (!warp_wait_bar(smem_u32(&bars->lempty[stage]), phase ^ 1u, abort_flag, lane)) { ok = false; break; }
                 const uint32_t fb = smem_u32(&bars->lfull[stage]);
-                const int grp = (kt * BK + half * (BK / 2)) / g;
-                const bool valid = n < N && grp < groups;
-                const size_t so = valid ? static_cast<size_t>(grp) * N + n : 0;
-                if constexpr (kMx) {
-                    cp_async_8(smem_u32(ld_s(stage)) + half * BN + 8 * sub, reinterpret_cast<const uint8_t*>(sc) + so,
-                               valid ? 8u : 0u);
-                } else {
-                    cp_async_16(smem_u32(ld_s(stage)) + half * (BN * 2) + 16 * sub, sc + so, valid ? 16u : 0u);
-                }
-                if constexpr (!kSym) {
-                    const size_t zo = valid ? static_cast<size_t>(grp) * (N >> 3) + (n >> 3) : 0;
-                    cp_async_4(smem_u32(ld_z(stage)) + half * (BN / 8) * 4 + 4 * sub, qz + zo, valid ? 4u : 0u);
+#pragma unroll
+                for (int p = 0; p < kSub; ++p) {
+                    const int qt = 2 * p + half;                 // 32-row block of the step
+                    const int grp = (kt * BK + qt * 32) / g;
+                    const bool valid = n < N && grp < groups;
+                    const size_t so = valid ? static_cast<size_t>(grp) * N + n : 0;
+                    if constexpr (kMx) {
+                        cp_async_8(smem_u32(ld_s(stage)) + qt * BN + 8 * sub, reinterpret_cast<const uint8_t*>(sc) + so,
+                                   valid ? 8u : 0u);
+                    } else {
+                        cp_async_16(smem_u32(ld_s(stage)) + qt * (BN * 2) + 16 * sub, sc + so, valid ? 16u : 0u);
+                    }
+                    if constexpr (!kSym) {
+                        const size_t zo = valid ? static_cast<size_t>(grp) * (N >> 3) + (n >> 3) : 0;
+                        cp_async_4(smem_u32(ld_z(stage)) + qt * (BN / 8) * 4 + 4 * sub, qz + zo, valid ? 4u : 0u);
+                    }
                 }
                 cp_async_mbar_arrive(fb);
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive_expect_tx(fb, C::kABytes + kWBytes);
-                    tma_load_2d(ld_a(stage), &tmap_x, kt * BK, 0, fb);
+#pragma unroll
+                    for (int p = 0; p < kSub; ++p)   // x in 64-column boxes (the 128-byte swizzle's width)
+                        tma_load_2d(ld_a(stage) + p * (MP * 128), &tmap_x, kt * BK + 64 * p, 0, fb);
                     tma_load_2d(smem_u32(ld_w(stage)), &tmap_w, n0, kt * (BK / 8), fb);
                 }
                 issued[stage] = true;
@@ -325,11 +347,14 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_cons
                     // which it starts only after the step's x tile has landed
                     if (!wait_bar(smem_u32(&bars->bfull[bs]), bph, abort_flag)) { ok = false; break; }
                     tc_fence_after();
-                    const uint64_t wdesc = sw128_kmajor_desc(op_w(bs));
-                    const uint64_t xdesc = sw128_kmajor_desc(ld_a(ls));
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk)
-                        umma_f16(d_tmem, wdesc + 2u * kk, xdesc + 2u * kk, kIdesc, (kt - k0) + kk != 0);
+                    for (int p = 0; p < kSub; ++p) {
+                        const uint64_t wdesc = sw128_kmajor_desc(op_w(bs) + p * kSubBytes);
+                        const uint64_t xdesc = sw128_kmajor_desc(ld_a(ls) + p * (MP * 128));
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            umma_f16(d_tmem, wdesc + 2u * kk, xdesc + 2u * kk, kIdesc, (kt - k0) + p + kk != 0);
+                    }
                     umma_commit(smem_u32(&bars->lempty[ls]));
                     umma_commit(smem_u32(&bars->bempty[bs]));
                     if (++ls == L) ls = 0;
@@ -440,7 +465,7 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_cons
         const int grp = tg >> 8;                         // group: steps j with j % kDeqGroups == grp
         const int td = tg & 255;
         const int d = td & (BN - 1);                     // column of the tile
-        const int half = td >> 7;                        // 32-row half of the step: words 4*half .. 4*half+3
+        const int tq = td >> 7;                          // this thread's 32-row blocks: kSub * tq .. kSub * tq + kSub - 1
         int ls = 0, bs = 0;
         uint32_t lph = 0, bph = 0;
         bool ok = true;
@@ -466,37 +491,39 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_cons
                 const uint32_t* wt = reinterpret_cast<const uint32_t*>(ld_w(ls));
                 const uint16_t* st = reinterpret_cast<const uint16_t*>(ld_s(ls));
                 const uint32_t* zt = reinterpret_cast<const uint32_t*>(ld_z(ls));
-                const uint32_t b_row = op_w(bs) + static_cast<uint32_t>(d) * 128u;
-                if constexpr (kMx) {
-                    mx::operand_column<BN>(wt, b_row, d, half, reinterpret_cast<const uint8_t*>(st)[half * BN + d]);
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(smem_u32(&bars->bfull[bs]));
-                    advance();
-                    continue;
-                }
-                const uint32_t s16 = st[half * BN + d];
-                const uint32_t z4 = kSym ? 8u : ((zt[half * (BN / 8) + (d >> 3)] >> (4 * (d & 7))) & 0xFu);
-                const uint32_t ss = s16 | (s16 << 16);
-                const uint32_t zz = Dq<kBf16>::kMagic | z4 | (z4 << 16);
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    const int c = half * 4 + cc;
-                    const uint32_t w = wt[c * BN + d];
-                    const uint32_t w4 = w >> 4;
-                    uint32_t o[4];
-#pragma unroll
-                    for (int b = 0; b < 4; ++b) {
-                        // byte b of w -> low half, byte b of (w >> 4) -> high half:
-                        // halves (magic + q[8c + 2b], magic + q[8c + 2b + 1])
-                        const uint32_t h = and_or(prmt(w, w4, static_cast<uint32_t>(b | ((4 + b) << 8))),
-                                                  0x000F000Fu, Dq<kBf16>::kMagic);
-                        o[b] = Dq<kBf16>::mul2(Dq<kBf16>::sub2(h, zz), ss);
+                for (int r = 0; r < kSub; ++r) {
+                    const int qt = tq * kSub + r;                // 32-row block: word rows 4*qt .. 4*qt+3
+                    const int p = qt >> 1, half = qt & 1;        // sub-tile, and half of its 64 rows
+                    const uint32_t* wp = wt + p * 8 * BN;        // the sub-tile's 8 word rows
+                    const uint32_t b_row = op_w(bs) + p * kSubBytes + static_cast<uint32_t>(d) * 128u;
+                    if constexpr (kMx) {
+                        mx::operand_column<BN>(wp, b_row, d, half, reinterpret_cast<const uint8_t*>(st)[qt * BN + d]);
+                        continue;
                     }
-                    const uint32_t dst = b_row + (static_cast<uint32_t>(c ^ (d & 7)) << 4);
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(o[0]), "r"(o[1]),
-                                 "r"(o[2]), "r"(o[3])
-                                 : "memory");
+                    const uint32_t s16 = st[qt * BN + d];
+                    const uint32_t z4 = kSym ? 8u : ((zt[qt * (BN / 8) + (d >> 3)] >> (4 * (d & 7))) & 0xFu);
+                    const uint32_t ss = s16 | (s16 << 16);
+                    const uint32_t zz = Dq<kBf16>::kMagic | z4 | (z4 << 16);
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) {
+                        const int c = half * 4 + cc;
+                        const uint32_t w = wp[c * BN + d];
+                        const uint32_t w4 = w >> 4;
+                        uint32_t o[4];
+#pragma unroll
+                        for (int b = 0; b < 4; ++b) {
+                            // byte b of w -> low half, byte b of (w >> 4) -> high half:
+                            // halves (magic + q[8c + 2b], magic + q[8c + 2b + 1])
+                            const uint32_t h = and_or(prmt(w, w4, static_cast<uint32_t>(b | ((4 + b) << 8))),
+                                                      0x000F000Fu, Dq<kBf16>::kMagic);
+                            o[b] = Dq<kBf16>::mul2(Dq<kBf16>::sub2(h, zz), ss);
+                        }
+                        const uint32_t dst = b_row + (static_cast<uint32_t>(c ^ (d & 7)) << 4);
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(o[0]), "r"(o[1]),
+                                     "r"(o[2]), "r"(o[3])
+                                     : "memory");
+                    }
                 }
                 // the MMA (async proxy) reads these writes
                 fence_proxy_async_smem();
@@ -530,8 +557,9 @@ cudaError_t launch_mp(const void* x, const uint32_t* qw, const void* sc, const u
     }
     CUtensorMap tx, tw;
     const CUtensorMapDataType adt = kBf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    if (!encode_2d(&tx, adt, x, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, BK, MP, CU_TENSOR_MAP_SWIZZLE_128B))
+    if (!encode_2d(&tx, adt, x, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, 64, MP, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
+    constexpr int BK = Cfg<MP>::BK;
     if (!encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_INT32, qw, (uint64_t)N, (uint64_t)(K / 8), (uint64_t)N * 4, BN,
                    BK / 8, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
