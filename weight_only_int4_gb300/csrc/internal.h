@@ -67,9 +67,10 @@ cudaError_t read_and_clear_device_error(uint32_t* out, cudaStream_t s);
 cudaError_t read_and_clear_gemv_error(uint32_t* out);
 cudaError_t launch_wait_selftest(cudaStream_t s);
 // GEMMs with at most this many rows of x run the operand-swapped kernel
-// (weights as the 128-row MMA operand, x padded to 32..128 rows); measured at
-// N = 43008, K = 5376: 154-160 us for M = 17..128 against 174-180 us on the
-// CTA-pair kernel, which wins from M = 192 on (180 vs 247 us).
+// (weights as the 128-row MMA operand, x padded to 32..128 rows; it cannot take
+// more); measured at N = 43008, K = 5376: 109-133 us for M = 1..128 against
+// 174-180 us on the CTA-pair kernel, which runs M >= 129 (180 us at M = 192,
+// where the operand-swapped kernel with 256 padded rows took 247 us).
 #ifndef W4A16_SKINNY_MAX_M
 #define W4A16_SKINNY_MAX_M 128
 #endif
