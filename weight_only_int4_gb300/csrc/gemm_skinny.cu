@@ -83,7 +83,10 @@ struct Cfg {
     static constexpr int BK = MP <= W4A16_SKINNY_BK128_MAX_MP ? 128 : 64;   // K per step
     static constexpr int kSub = BK / 64;            // 64-deep sub-tiles per step (one 128-byte swizzle row each)
     static constexpr int kQuarters = BK / 32;       // 32-row scale blocks per step
-    static constexpr int kBStages = BK == 128 ? 2 : 4;
+#ifndef W4A16_SKINNY_BK128_B_STAGES
+#define W4A16_SKINNY_BK128_B_STAGES 2
+#endif
+    static constexpr int kBStages = BK == 128 ? W4A16_SKINNY_BK128_B_STAGES : 4;
     static constexpr uint32_t kWBytes = (BK / 8) * BN * 4;          // packed weights
     static constexpr uint32_t kSBytes = kQuarters * BN * 2;         // scales of the step's 32-row blocks
     static constexpr uint32_t kZBytes = kQuarters * (BN / 8) * 4;   // zero-point words of the blocks
