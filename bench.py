@@ -1,8 +1,8 @@
 """Benchmark of the W4A16 layer on one GB300 (or N replicas under torchrun).
 
-A step is one decode pass over L layers: L launches of the GEMV, each on its
-own copy of the packed weights (so every launch streams its weights from HBM,
-not L2). The headline workload is the gate_up-like decode GEMV
+A step is one decode pass over L layers (32 by default): L launches of the
+GEMV, each on its own copy of the packed weights (so every launch streams its
+weights from HBM, not L2), replayed as one CUDA graph. The headline workload is the gate_up-like decode GEMV
 1 x 43008 x 5376, g=32, fp16, asymmetric; the same run also times the prefill
 GEMM 2048 x 43008 x 5376, g=32, bf16 ("prefill" object).
 
@@ -387,7 +387,7 @@ def run_ours(args, rank, world, barrier, allmax):
 
     wl = WORKLOADS[args.workload]
     per_layer = layer_bytes(wl.M, wl.N, wl.K, wl.g, wl.symmetric, wl.act).total
-    L = copies_for(per_layer, l2)
+    L = max(copies_for(per_layer, l2), args.layers)
     copy_gbs = box_copy_gbs(torch)
     layer = Layer(args.workload, L, torch, w4)
 
@@ -425,6 +425,8 @@ def run_ours(args, rank, world, barrier, allmax):
         "data": "synthetic (seeded: x~N(0,1), q,z~U{0..15}, s~U[0.002,0.02])",
         "config": {"workload": args.workload, "M": wl.M, "N": wl.N, "K": wl.K, "g": wl.g,
                    "layers_per_step": L, "parallelism": f"replicas x{world}",
+                   "step": f"one CUDA graph of {L} GEMV calls on distinct weight copies (a decode step of "
+                           f"{L} layers' gate_up projections)",
                    "l2": f"each step streams {L} distinct weight copies "
                          f"({L * per_layer / 1e6:.0f} MB > L2 {l2 / 1e6:.0f} MB)",
                    "timing": "CUDA-graph replay of one step, CUDA events on the replay stream"},
@@ -557,6 +559,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DECODE, choices=[n for n, w in WORKLOADS.items() if w.kernel == "gemv"])
+    ap.add_argument("--layers", type=int, default=32,
+                    help="layers (distinct weight copies) per decode step, like one decode step of a 32-layer "
+                         "decoder captured as one graph; at least enough to exceed 4x L2")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
