@@ -31,7 +31,6 @@ namespace mx {
 
 constexpr int kBlock = 32;                      // K rows per E8M0 byte
 constexpr uint32_t kTwoPow126x2 = 0x7E807E80u;  // bf16 2^126 in both halves
-constexpr uint32_t kOneX2 = 0x3F803F80u;        // bf16 1.0 in both halves
 
 // Two codes, in bits 0..3 of each 16-bit half (all other bits zero), to the
 // bf16 patterns of E2M1(c) * 2^-126: (c << 6) places m, E at bits 6..8 and
