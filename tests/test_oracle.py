@@ -4,7 +4,7 @@ import pytest
 
 import oracle_pins as P
 from oracle import w4a16_oracle as O
-from w4a16_inputs import make_case
+from w4a16_inputs import make_case, make_large_case
 
 
 @pytest.mark.parametrize("pin", P.ALL_PINS, ids=lambda f: f.__name__)
@@ -84,6 +84,22 @@ def test_sampled_rows_and_cols_match_full():
                        rtol=1e-13, atol=1e-13)
     assert np.allclose(O.reference_cols(case.x, cols, qw, case.s, qz, 128, "bf16"), full[:, cols],
                        rtol=1e-13, atol=1e-13)
+
+
+def test_column_blocks_sliced_from_the_operands():
+    """Output columns depend only on their own operands: the layer on 8-column
+    blocks cut out of qweight, scales and the packed zero-point words (whole
+    words) equals those columns of the full layer. The large GPU tests check
+    sampled columns this way."""
+    case = make_large_case(5, 272, 512, 128, "bf16", seed=3, device="cpu")
+    blocks = [0, 17, 33]
+    cols = np.concatenate([np.arange(8 * b, 8 * b + 8) for b in blocks])
+    qw = case.qw.numpy()
+    zw = case.zw.view(np.int32)
+    full = O.reference(case.x, qw, case.s, zw, 128, "bf16")
+    part = O.reference(case.x, np.ascontiguousarray(qw[:, cols]), np.ascontiguousarray(case.s[:, cols]),
+                       np.ascontiguousarray(zw[:, blocks]), 128, "bf16")
+    assert np.array_equal(part, full[:, cols])
 
 
 def test_rejects_bad_operands():

@@ -4,7 +4,9 @@ This module is shared by the tests, the benchmark and the CPU oracle. It only
 draws random numbers and stores them in the operand dtypes; it holds none of
 the layer's arithmetic (no packing, no dequantisation, no matmul). Both the
 CUDA path and the oracle pack the unpacked 4-bit codes drawn here with their
-own, independent packers.
+own, independent packers. At the largest sizes the packed words themselves are
+drawn instead (on the device): a uniformly random 32-bit word is eight
+independent uniform codes, so neither side packs anything.
 
 Value distributions follow the decode and prefill workloads of "Keep W4A16
 zero-points packed at 4 bits instead of expanding to 2 bytes" (§Problem,
@@ -35,6 +37,10 @@ __all__ = [
     "f32_to_act",
     "make_case",
     "make_case_for",
+    "LargeCase",
+    "make_large_case",
+    "make_large_mx_case",
+    "device_codes",
 ]
 
 ACT_DTYPES = ("f16", "bf16")
@@ -224,3 +230,77 @@ MX_WORKLOADS = {w.name: w for w in [
     MxWorkload("mx_gemm_64x43008x5376_bf16", "gemm", 64, 43008, 5376),
     MxWorkload("mx_dequant_43008x5376_bf16", "dequant", 1, 43008, 5376),
 ]}
+
+
+# ---------------------------------------------------------------------------
+# Cases at the largest sizes: weights drawn as packed words on the device
+# ---------------------------------------------------------------------------
+def _device_generator(seed: int, device):
+    import torch
+    return torch.Generator(device=device).manual_seed(seed)
+
+
+def device_words(shape, seed: int, device="cuda"):
+    """Uniformly random 32-bit words (torch.int32) drawn on `device` by torch's
+    seeded generator. A uniform word holds eight independent codes uniform on
+    0..15 whichever nibble order reads it, so packed operands of any size can be
+    drawn without packing anything."""
+    import torch
+    return torch.randint(-2 ** 31, 2 ** 31, tuple(shape), dtype=torch.int32, device=device,
+                         generator=_device_generator(seed, device))
+
+
+def device_codes(shape, seed: int, device="cuda"):
+    """Codes uniform on 0..15 (torch.uint8) drawn on `device`."""
+    import torch
+    return torch.randint(0, 16, tuple(shape), dtype=torch.uint8, device=device,
+                         generator=_device_generator(seed, device))
+
+
+@dataclass
+class LargeCase:
+    """A problem too large to draw code by code on the host.
+
+    x  : [M, K] activations in `act` (host)
+    s  : [K/g, N] scales in `act` (host); for MXFP4, E8M0 bytes [K/32, N]
+    zw : [K/g, N/8] uint32 zero-point words (host; eight codes each), or None
+    qw : [K/8, N] int32 weight words on the device (eight codes each)
+    """
+
+    M: int
+    N: int
+    K: int
+    g: int
+    act: str
+    x: np.ndarray
+    s: np.ndarray
+    zw: Optional[np.ndarray]
+    qw: object
+
+
+def make_large_case(M: int, N: int, K: int, g: int, act: str = "bf16", symmetric: bool = False,
+                    seed: int = 0, device="cuda") -> LargeCase:
+    """Same distributions as make_case (x ~ N(0, 1), codes and zero-points
+    uniform on 0..15, scales uniform on [0.002, 0.02]); x, s and the zero-point
+    words from one numpy PCG64 stream, the weight words on the device."""
+    if act not in ACT_DTYPES or M < 0 or N < 8 or N % 8 or K < g or K % g or K % 8:
+        raise ValueError(f"bad shape M={M} N={N} K={K} g={g} act={act}")
+    rng = np.random.Generator(np.random.PCG64(seed))
+    x32 = rng.standard_normal((M, K), dtype=np.float32)
+    s32 = np.float32(0.002) + np.float32(0.018) * rng.random((K // g, N), dtype=np.float32)
+    zw = None if symmetric else rng.integers(0, 2 ** 32, size=(K // g, N // 8), dtype=np.uint32)
+    return LargeCase(M=M, N=N, K=K, g=g, act=act, x=f32_to_act(x32, act), s=f32_to_act(s32, act), zw=zw,
+                     qw=device_words((K // 8, N), seed + 1, device))
+
+
+def make_large_mx_case(M: int, N: int, K: int, seed: int = 0, device="cuda") -> LargeCase:
+    """MXFP4 counterpart: bf16 x ~ N(0, 1), E2M1 codes uniform, exponent bytes
+    uniform on 118..125 ("typical")."""
+    if M < 0 or N < 16 or N % 16 or K < 32 or K % 32:
+        raise ValueError(f"bad MXFP4 shape M={M} N={N} K={K}")
+    lo, hi = _MX_EXPONENTS["typical"]
+    rng = np.random.Generator(np.random.PCG64(seed))
+    x32 = rng.standard_normal((M, K), dtype=np.float32)
+    e = rng.integers(lo, hi + 1, size=(K // 32, N), dtype=np.uint8)
+    return LargeCase(M=M, N=N, K=K, g=32, act="bf16", x=f32_to_act(x32, "bf16"), s=e, zw=None,
+                     qw=device_words((K // 8, N), seed + 1, device))
