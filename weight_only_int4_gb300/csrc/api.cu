@@ -4,7 +4,9 @@
 
 #include "internal.h"
 
+#include <map>
 #include <mutex>
+#include <utility>
 
 namespace w4a16 {
 
@@ -29,6 +31,18 @@ cudaError_t current_device_props(DeviceProps* out) {
     }
     *out = cache[dev];
     return cudaSuccess;
+}
+
+cudaError_t ensure_dynamic_smem(const void* kernel, int device, size_t bytes) {
+    static std::mutex mu;
+    static std::map<std::pair<const void*, int>, size_t> set;   // largest limit set per (kernel, device)
+    std::lock_guard<std::mutex> lock(mu);
+    size_t& cur = set[{kernel, device}];
+    if (cur >= bytes) return cudaSuccess;
+    const cudaError_t e =
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+    if (e == cudaSuccess) cur = bytes;
+    return e;
 }
 
 }  // namespace w4a16

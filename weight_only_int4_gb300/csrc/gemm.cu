@@ -555,13 +555,9 @@ template <bool kBf16, bool kSym, bool kMx = false>
 cudaError_t launch_typed(const void* x, const uint32_t* qw, const void* sc, const uint32_t* qz, void* y, int M,
                          int N, int K, int g, const DeviceProps& dp, cudaStream_t s) {
     auto kern = gemm_kernel<kBf16, kSym, kMx>;
-    static int configured_device[64] = {0};
-    if (dp.device >= 0 && dp.device < 64 && !configured_device[dp.device]) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(kSmemBytes));
-        if (e != cudaSuccess) return e;
-        configured_device[dp.device] = 1;
-    }
+    if (cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), dp.device, kSmemBytes);
+        e != cudaSuccess)
+        return e;
     CUtensorMap tx, tw;
     const CUtensorMapDataType adt = kBf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     if (!encode_2d(&tx, adt, x, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, BK, CM,

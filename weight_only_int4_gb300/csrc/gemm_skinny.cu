@@ -552,12 +552,8 @@ cudaError_t launch_mp(const void* x, const uint32_t* qw, const void* sc, const u
     auto kern = gemm_skinny_kernel<kBf16, kSym, MP, kMx>;
     constexpr size_t kSmem = smem_bytes<MP>();
     static_assert(kSmem <= 227 * 1024, "shared memory budget");
-    static int configured_device[64] = {0};
-    if (dp.device >= 0 && dp.device < 64 && !configured_device[dp.device]) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmem));
-        if (e != cudaSuccess) return e;
-        configured_device[dp.device] = 1;
-    }
+    if (cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), dp.device, kSmem); e != cudaSuccess)
+        return e;
     CUtensorMap tx, tw;
     const CUtensorMapDataType adt = kBf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     if (!encode_2d(&tx, adt, x, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, 64, MP, CU_TENSOR_MAP_SWIZZLE_128B))

@@ -642,12 +642,9 @@ cudaError_t launch_one(const GemvArgs& a, const GemvPlan& p, cudaStream_t s) {
     static_assert(Stage<COLS, MT>::kBytes == stage_bytes(COLS, MT), "stage layout");
     auto kern = gemv_kernel<kBf16, MT, COLS, kSym, kFact, kZBulk, kMx, kXPre>;
     const size_t smem = p.smem_bytes;
-    static size_t configured[64] = {0};   // largest dynamic shared memory set, per device
-    const int dev = p.device;
-    if (smem > 48 * 1024 && (dev < 0 || dev >= 64 || configured[dev] < smem)) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < 64) configured[dev] = smem;
+    if (smem > 48 * 1024) {
+        if (cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), p.device, smem); e != cudaSuccess)
+            return e;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.grid);

@@ -17,6 +17,12 @@ struct DeviceProps {
 // Properties of the current device, cached per device ordinal.
 cudaError_t current_device_props(DeviceProps* out);
 
+// Raise `kernel`'s dynamic shared memory limit on `device` (the current
+// device) to at least `bytes`. Thread-safe; the limit only ever grows, so a
+// launch that needs less is never refused because another thread set a
+// smaller limit in between.
+cudaError_t ensure_dynamic_smem(const void* kernel, int device, size_t bytes);
+
 cudaError_t launch_pack(const uint8_t* src, uint32_t* dst, int64_t rows, int64_t cols, int dim,
                         const DeviceProps& dp, cudaStream_t s);
 cudaError_t launch_unpack(const uint32_t* src, uint8_t* dst, int64_t rows, int64_t cols, int dim,
