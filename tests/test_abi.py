@@ -185,3 +185,10 @@ def test_binding_rejects_activation_dtype_zero_points():
     # CPU tensors are rejected before any dtype reasoning reaches the library
     with pytest.raises(ValueError):
         w4.gemv(x, qw, s, z_expanded, 32)
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    """Without libw4a16.so the binding raises; there is no fallback path."""
+    monkeypatch.setattr(w4, "_lib", None)
+    with pytest.raises(RuntimeError, match="libw4a16.so not found"):
+        w4.load_library(str(tmp_path / "libw4a16.so"))
