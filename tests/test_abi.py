@@ -1,6 +1,5 @@
 """CPU checks of the C ABI: the library loads, exports every declared symbol,
 and rejects bad arguments on the host before anything reaches a device."""
-import ctypes
 import os
 import re
 
