@@ -42,7 +42,9 @@
  *   - The library runs only on compute capability 10.3 (GB300); any other
  *     device gives W4A16_ERR_DEVICE.
  *   - Shape limits: N % 8 == 0, K % g == 0, g in {32, 64, 128, 256}, all
- *     dimensions > 0 and < 2^31, base pointers 16-byte aligned.
+ *     dimensions > 0 and < 2^31, base pointers 16-byte aligned. Products of
+ *     dimensions are not limited: every offset is computed in 64 bits, so
+ *     tensors past 2^32 elements or 4 GiB are fine.
  */
 #ifndef W4A16_H
 #define W4A16_H
