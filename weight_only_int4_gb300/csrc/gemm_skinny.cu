@@ -3,7 +3,7 @@
 //
 // For small M the weights dominate everything: the layer must stream and
 // dequantise K*N weights whatever M is, while the MMA work shrinks with M.
-// Here each CTA owns 128 weight columns (one column block) and all M rows:
+// Here the unit of work is a 128-column block of weights with all M rows:
 // the dequantised weight tile [128 x 64] is the MMA's A operand (M_mma = 128),
 // the x tile [MP x 64] its B operand (N_mma = MP, M rounded up to a multiple
 // of 32), and each CTA's tensor memory holds D[n][m] = y[m][n] for its
@@ -18,10 +18,11 @@
 // so every SM dequantises the same number of steps whatever the number of
 // column blocks (336 blocks over 152 SMs would otherwise leave a third of the
 // SMs idle in the last round). A column block whose steps are split between
-// CTAs is finished by the last of them to arrive: each writes its FP32
-// partial [M x 128] to a workspace slot, takes the block's ticket, and the
-// last one sums the partials in ascending CTA order (deterministic) and
-// stores y.
+// CTAs is finished per epilogue warp (32 columns) by the last contributor to
+// arrive: each writes its FP32 partial (column-major, rows contiguous) to a
+// workspace slot, takes the (block, warp) ticket, and the last one sums the
+// partials in ascending CTA order (deterministic), stores y and resets the
+// ticket.
 //
 // Warp roles, one CTA per SM, each walking the CTA's (column block, K range)
 // segments in order:
