@@ -191,3 +191,9 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(w4, "_lib", None)
     with pytest.raises(RuntimeError, match="libw4a16.so not found"):
         w4.load_library(str(tmp_path / "libw4a16.so"))
+
+
+def test_release_workspaces_drops_the_cache(monkeypatch):
+    monkeypatch.setattr(w4, "_workspaces", {(0, 0, w4.OP_GEMV): object()})
+    w4.release_workspaces()
+    assert w4._workspaces == {}

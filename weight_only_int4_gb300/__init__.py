@@ -188,6 +188,13 @@ def _cached_workspace(nbytes: int, device, stream_ptr: int, op: int):
     return ws
 
 
+def release_workspaces() -> None:
+    """Drop the workspaces the binding allocated for calls made without one (one
+    per device, stream and op). Call it only when no such call is in flight on
+    the device; the next call allocates a fresh, zeroed workspace."""
+    _workspaces.clear()
+
+
 def _layer(fn_name: str, x, qweight, scales, qzeros, group_size: int, out=None, workspace=None,
            stream=None):
     torch = _torch()
