@@ -211,8 +211,10 @@ class MxLayer:
                 self.fn(x, qw, e, out=y, workspace=self.ws)
 
 
-def time_graph(layer, steps, warmup, torch, barrier):
-    """Device time of `steps` replays of a CUDA graph of one step (events on the replay stream)."""
+def time_graph(layer, steps, warmup, torch, barrier, per_step=None):
+    """Device time of `steps` replays of a CUDA graph of one step (events on the
+    replay stream). An event follows every replay, so `per_step` (a list, if
+    given) receives each replay's own time; their sum is the total returned."""
     stream = torch.cuda.Stream()
     for _ in range(max(1, warmup)):
         layer.step()
@@ -225,16 +227,17 @@ def time_graph(layer, steps, warmup, torch, barrier):
     torch.cuda.synchronize()
     barrier()
     torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
     with torch.cuda.stream(stream):
-        t0 = torch.cuda.Event(enable_timing=True)
-        t1 = torch.cuda.Event(enable_timing=True)
-        t0.record(stream)
-        for _ in range(steps):
+        ev[0].record(stream)
+        for i in range(steps):
             g.replay()
-        t1.record(stream)
+            ev[i + 1].record(stream)
     torch.cuda.synchronize()
     barrier()
-    return t0.elapsed_time(t1) / 1e3   # seconds
+    if per_step is not None:
+        per_step.extend(ev[i].elapsed_time(ev[i + 1]) / 1e3 for i in range(steps))
+    return ev[0].elapsed_time(ev[steps]) / 1e3   # seconds
 
 
 def time_graph_samples(layer, steps, warmup, torch):
@@ -363,6 +366,47 @@ def box_copy_gbs(torch, nbytes=1 << 30, reps=5):
     return round(gbs, 1)
 
 
+# The decode workloads the metric names beside the headline (M = 1-4): the
+# 1x2048x2048 g=128 case, the M = 4 g=128 sweep in fp16 and bf16, and the
+# qkv-like and down-like shapes, symmetric and asymmetric.
+METRIC_CONFIGS = [
+    "gemv_1x2048x2048_g128_f16_asym",
+    "gemv_4x2048x2048_g128_f16_asym", "gemv_4x2048x2560_g128_f16_asym",
+    "gemv_4x6144x2048_g128_f16_asym", "gemv_4x4096x2048_g128_f16_asym",
+    "gemv_4x2048x2048_g128_bf16_asym", "gemv_4x2048x2560_g128_bf16_asym",
+    "gemv_4x6144x2048_g128_bf16_asym", "gemv_4x4096x2048_g128_bf16_asym",
+    "gemv_1x16384x5376_g32_bf16_sym", "gemv_1x16384x5376_g32_bf16_asym",
+    "gemv_1x5376x21504_g32_bf16_sym", "gemv_1x5376x21504_g32_bf16_asym",
+]
+NOMINAL_HBM_GBS = 8000.0
+
+
+def time_metric_configs(names, replays, warmup, torch, w4, peaks, l2):
+    """Median and min time per call of each named decode workload: `replays`
+    CUDA-graph replays of L calls on distinct weight copies (L such that one
+    replay streams >= 4x L2, so every call reads its weights from HBM)."""
+    rows = []
+    for name in names:
+        wl = WORKLOADS[name]
+        per = layer_bytes(wl.M, wl.N, wl.K, wl.g, wl.symmetric, wl.act).total
+        L = copies_for(per, l2)
+        layer = Layer(name, L, torch, w4)
+        t = []
+        time_graph(layer, replays, warmup, torch, lambda: None, per_step=t)
+        t = [v / L for v in t]
+        med, mn = statistics.median(t), min(t)
+        rows.append({"workload": name, "M": wl.M, "N": wl.N, "K": wl.K, "g": wl.g, "dtype": wl.act,
+                     "calls_per_replay": L, "replays": replays,
+                     "us_median": round(med * 1e6, 3), "us_min": round(mn * 1e6, 3),
+                     "GBs_median": round(per / med / 1e9, 1),
+                     "frac_measured_hbm": round(per / med / 1e9 / peaks["hbm_gbs"], 4),
+                     "frac_nominal_8tbs": round(per / med / 1e9 / NOMINAL_HBM_GBS, 4),
+                     "algorithmic_bytes_per_call": per})
+        del layer
+        torch.cuda.empty_cache()
+    return rows
+
+
 def copies_for(bytes_per_layer, l2_bytes):
     """Enough weight copies that one step moves >= 1 GB and >= 4x L2."""
     target = max(1e9, 4 * l2_bytes)
@@ -393,7 +437,8 @@ def run_ours(args, rank, world, barrier, allmax):
 
     clocks = ClockSampler(local)
     clocks.start()
-    secs = time_graph(layer, args.steps, args.warmup, torch, barrier)
+    step_s = []
+    secs = time_graph(layer, args.steps, args.warmup, torch, barrier, per_step=step_s)
     clk = clocks.stop()
     secs = allmax(secs)
     launches = args.steps * L
@@ -436,6 +481,9 @@ def run_ours(args, rank, world, barrier, allmax):
                      "traffic": load_traffic("gemv", args.workload),
                      "kernel": "gemv_kernel", "algorithmic_bytes_per_launch": bytes_per_launch,
                      "us_per_launch": round(launch_s * 1e6, 3),
+                     "us_per_launch_median": round(statistics.median(step_s) / L * 1e6, 3),
+                     "us_per_launch_min": round(min(step_s) / L * 1e6, 3),
+                     "frac_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
                      "context": {"this_gpu_copy_gbs": copy_gbs,
                                  "frac_of_this_gpu_copy": round(achieved / copy_gbs, 4)}},
         "clocks": clk,
@@ -446,6 +494,17 @@ def run_ours(args, rank, world, barrier, allmax):
     }
     del layer
     torch.cuda.empty_cache()
+
+    if not args.no_configs:
+        clocks = ClockSampler(local)
+        clocks.start()
+        rows = time_metric_configs(METRIC_CONFIGS, max(50, args.config_replays), max(3, args.warmup), torch,
+                                   w4, peaks, l2)
+        cclk = clocks.stop()
+        line["configs"] = {"rows": rows, "clocks": cclk, "peak_source": peak_src,
+                           "timing": "per-replay CUDA events around a CUDA graph of L calls on distinct "
+                                     "weight copies; per call = replay / L; median and min over the replays"}
+        line["gpu_launches"] += sum(r["calls_per_replay"] * r["replays"] for r in rows)
 
     if not args.no_prefill:
         pw = WORKLOADS[PREFILL]
@@ -491,7 +550,32 @@ def oracle_sample(name, cols):
     return wl, case.x, O.pack_rows(q), s, (None if z is None else O.pack_cols(z))
 
 
-def cpu_baseline(name, budget_s=15.0, cols=2048):
+# Output columns of the workload in the oracle's sample; the CPU baseline of
+# the default line and the reference arm time the same sample.
+ORACLE_COLS = 1024
+
+
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
+
+
+def cpu_baseline(name, budget_s=15.0, cols=ORACLE_COLS):
     from oracle import w4a16_oracle as O
     wl, x, qw, s, qz = oracle_sample(name, cols)
     bytes_sample = layer_bytes(wl.M, cols, wl.K, wl.g, wl.symmetric, wl.act).total
@@ -505,12 +589,12 @@ def cpu_baseline(name, budget_s=15.0, cols=2048):
     return {"value": round(n * bytes_sample / t_wall / 1e9, 4), "unit": "GB/s",
             "cores": max(1, round(t_cpu / t_wall)), "kind": "oracle",
             "sample": f"{n} x oracle on columns [0,{cols}) of {name} ({bytes_sample} B each)",
-            "host_cpus": os.cpu_count()}
+            "host_cpus": os.cpu_count(), "cpu_model": cpu_model()}
 
 
 def run_reference(args):
     from oracle import w4a16_oracle as O
-    cols = 1024
+    cols = ORACLE_COLS
     wl, x, qw, s, qz = oracle_sample(args.workload, cols)
     bytes_sample = layer_bytes(wl.M, cols, wl.K, wl.g, wl.symmetric, wl.act).total
     for _ in range(args.warmup):
@@ -529,7 +613,8 @@ def run_reference(args):
         "data": "synthetic (seeded)", "config": {"workload": args.workload, "M": wl.M, "N": wl.N, "K": wl.K,
                                                   "g": wl.g},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": max(1, round(cpu / wall)),
-                         "kind": "oracle", "sample": sample},
+                         "kind": "oracle", "sample": sample, "host_cpus": os.cpu_count(),
+                         "cpu_model": cpu_model()},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -564,6 +649,10 @@ def main():
                          "decoder captured as one graph; at least enough to exceed 4x L2")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-config rows (M = 1-4 decode workloads beside the headline)")
+    ap.add_argument("--config-replays", type=int, default=60,
+                    help="CUDA-graph replays per config row (at least 50)")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--configs", action="store_true", help="time every named workload (one GPU) and exit")
     ap.add_argument("--match", default="", help="with --configs: only workloads whose name contains this")

@@ -115,7 +115,7 @@ w4a16_status w4a16_unpack(const int32_t* src, uint8_t* dst, int64_t rows, int64_
 /*
  * w4a16_workspace_bytes -- bytes of device workspace `op` needs for this shape
  * on the current device. For the GEMV: a region of FP32 partial-sum slots
- * whose size depends only on the device (16 KB per SM), followed by one 32-bit
+ * whose size depends only on the device (8 KB per SM), followed by one 32-bit
  * ticket per column block of the shape (rounded up to 256 bytes). For the GEMM
  * with M <= 128: FP32 partial slots of 128 KB per SM, followed by four 32-bit
  * tickets per 128 columns (rounded up to 256 bytes); 0 for the GEMM with
@@ -186,15 +186,18 @@ w4a16_status w4a16_gemv(const void* x, const int32_t* qweight, const void* scale
  *   exits.
  * - The first call on a device looks up the array's device address once
  *   (cudaGetSymbolAddress, with that device current); make that first call
- *   before any stream capture on the device.
+ *   before any stream capture on the device. A first call made while `stream`
+ *   is being captured does not look the address up: it returns
+ *   W4A16_ERR_CUDA and enqueues nothing.
  * - Every call on a device uses the same array and clears its ticket words
  *   (an asynchronous memset on `stream`) before the kernel. Two calls that can
  *   run at the same time on one device (different streams) race on the array
  *   and give wrong results: serialise them.
  * - A shape whose scratch (w4a16_workspace_bytes(W4A16_OP_GEMV, ...)) exceeds
  *   4 MiB is rejected with W4A16_ERR_WORKSPACE; the partial-sum region takes
- *   16 KB per SM and each column block a 4-byte ticket, so on a 152-SM GB300
- *   this allows N up to about 13 million.
+ *   8 KB per SM and each column block a 4-byte ticket (column blocks are 32
+ *   columns wide for 9 <= M <= 16 and wider for smaller M), so on a 152-SM
+ *   GB300 every N up to about 23 million columns fits.
  * Results are identical to w4a16_gemv's for the same inputs. Other errors as
  * for w4a16_gemv.
  */

@@ -1,0 +1,43 @@
+"""Decode GEMV parity with skewed, mostly positive activations.
+
+For M <= 4 the GEMV applies the zero-point once per 32-row chunk through the
+chunk's sum of x: sum (q - z) x = sum (magic + q) x - (magic + z) sum x, a
+difference of two FP32 sums far larger than the result. Zero-mean x keeps the
+chunk sums small; activations after SiLU or GELU are mostly positive, which
+makes them, and the cancellation, largest. "qsa_prompt_attn: Q4_0 KV on tensor
+cores" (§Measured, "A bug the tests caught") records a real bug that a narrow
+input distribution hid. These cases draw x = 4 + N(0, 1) and x = 3 |N(0, 1)|
+on the decode shapes of "Keep W4A16 zero-points packed at 4 bits instead of
+expanding to 2 bytes" (§Results: gate_up, qkv, down) and compare every output
+of M = 1..4 with the FP64 oracle at the parity tolerance.
+"""
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import weight_only_int4_gb300 as w4  # noqa: E402
+from gpu_util import DeviceCase, assert_within_tol  # noqa: E402
+from w4a16_inputs import make_case  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+SHAPES = {
+    "gate_up_f16": (43008, 5376, 32, "f16", False),
+    "qkv_bf16": (16384, 5376, 32, "bf16", False),
+    "down_bf16": (5376, 21504, 32, "bf16", False),
+    "down_bf16_sym": (5376, 21504, 32, "bf16", True),
+    "g128_f16": (6144, 2048, 128, "f16", False),
+}
+
+
+@pytest.mark.parametrize("dist", ["offset", "halfnormal"])
+@pytest.mark.parametrize("shape", list(SHAPES))
+def test_skewed_activations(shape, dist):
+    N, K, g, act, sym = SHAPES[shape]
+    dc = DeviceCase(make_case(4, N, K, g, act, sym, seed=11, x_dist=dist))
+    ref = dc.reference()   # rows are independent: the first m rows serve M = m
+    for m in (1, 2, 3, 4):
+        y = w4.gemv(dc.x[:m], dc.qw, dc.s, dc.qz, g)
+        torch.cuda.synchronize()
+        assert_within_tol(y, ref[:m], act, f"{shape} {dist} M={m}")
+    assert w4.device_status() == w4.OK

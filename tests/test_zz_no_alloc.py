@@ -5,9 +5,11 @@ host program that owns all device memory, a serving process whose memory is
 already reserved, a loop where cudaMalloc's synchronisation is not allowed).
 For them the library keeps a fixed scratch array on the device and this entry
 point takes no workspace. These tests call it through the C ABI and check that
-it gives the same outputs as w4a16_gemv, on two calls in a row (the array keeps
-the previous call's contents, so the second call checks that nothing leaks
-from one call into the next). This file is collected last.
+it gives the same outputs as w4a16_gemv, bit for bit (both run the same plan
+and sum split column blocks in the same fixed order), on two calls in a row
+(the array keeps the previous call's contents, so the second call checks that
+nothing leaks from one call into the next), and, on one case, that it matches
+the FP64 oracle within the parity tolerance. This file is collected last.
 """
 import numpy as np
 import pytest
@@ -15,7 +17,7 @@ import pytest
 torch = pytest.importorskip("torch")
 
 import weight_only_int4_gb300 as w4  # noqa: E402
-from gpu_util import TOL, DeviceCase, torch_to_f64  # noqa: E402
+from gpu_util import TOL, DeviceCase, assert_within_tol, torch_to_f64  # noqa: E402
 from w4a16_inputs import make_case  # noqa: E402
 
 pytestmark = pytest.mark.gpu
@@ -53,6 +55,19 @@ def test_noalloc_matches_gemv_on_two_calls(M, N, K, g, act, sym):
         got = torch_to_f64(y)
         assert np.all(np.isfinite(got))
         assert np.abs(got - ref).max() <= TOL[act] * scale
+        assert torch.equal(y, y_ref), "w4a16_gemv_noalloc differs from w4a16_gemv"
+    assert w4.device_status() == w4.OK
+
+
+def test_noalloc_matches_oracle():
+    """One case through the oracle as well: two calls, each within the parity tolerance."""
+    dc = DeviceCase(make_case(2, 1032, 2048, 128, "bf16", False, seed=7))
+    ref = dc.reference()
+    for _ in range(2):
+        y = torch.full((2, 1032), float("nan"), dtype=torch.bfloat16, device="cuda")
+        assert call_noalloc(dc, y) == w4.OK
+        torch.cuda.synchronize()
+        assert_within_tol(y, ref, "bf16", "noalloc vs oracle")
     assert w4.device_status() == w4.OK
 
 

@@ -92,15 +92,24 @@ class Case:
 
 
 def make_case(M: int, N: int, K: int, g: int, act: str = "f16", symmetric: bool = False,
-              seed: int = 0, scales: str = "uniform") -> Case:
+              seed: int = 0, scales: str = "uniform", x_dist: str = "normal") -> Case:
     """Draw one case. `scales` is "uniform" (U[0.002, 0.02]) or "signed"
-    (random sign, magnitude log-uniform over [0.002, 0.2])."""
+    (random sign, magnitude log-uniform over [0.002, 0.2]). `x_dist` is
+    "normal" (N(0, 1)), or one of two skewed, mostly positive activation
+    shapes such as a SiLU or GELU output has: "offset" (4 + N(0, 1)) and
+    "halfnormal" (3 |N(0, 1)|). All three take the same draws from the stream."""
     if act not in ACT_DTYPES:
         raise ValueError(f"unknown activation dtype {act!r}")
     if M < 0 or N < 0 or K < 0 or g <= 0 or K % g:
         raise ValueError(f"bad shape M={M} N={N} K={K} g={g}")
     rng = np.random.Generator(np.random.PCG64(seed))
     x32 = rng.standard_normal((M, K), dtype=np.float32)
+    if x_dist == "offset":
+        x32 = x32 + np.float32(4.0)
+    elif x_dist == "halfnormal":
+        x32 = np.abs(x32) * np.float32(3.0)
+    elif x_dist != "normal":
+        raise ValueError(f"unknown activation distribution {x_dist!r}")
     q = rng.integers(0, 16, size=(K, N), dtype=np.uint8)
     if scales == "uniform":
         s32 = (np.float32(0.002) + np.float32(0.018) * rng.random((K // g, N), dtype=np.float32))

@@ -175,24 +175,41 @@ def new_workspace(nbytes: int, device=None):
 
 
 _workspaces = {}
+_retired = []
 
 
-def _cached_workspace(nbytes: int, device, stream_ptr: int, op: int):
+def _cached_workspace(nbytes: int, device, stream, op: int):
     """One growing workspace per (device, stream, op): calls on one stream never
-    overlap, and the GEMV and the GEMM lay out their workspaces differently."""
-    key = (device.index if device.index is not None else _torch().cuda.current_device(), stream_ptr, op)
+    overlap, and the GEMV and the GEMM lay out their workspaces differently.
+
+    The workspace is allocated and zero-filled on the stream the call runs on,
+    so the zero fill is ordered before the kernel and the caching allocator
+    ties the memory to that stream. A workspace outgrown by a larger shape is
+    kept alive (not freed) until release_workspaces(): a CUDA graph captured
+    through an earlier call may still replay into it."""
+    torch = _torch()
+    dev = device.index if device.index is not None else torch.cuda.current_device()
+    s = torch.cuda.current_stream(dev) if stream is None else stream
+    key = (dev, int(s.cuda_stream), op)
     ws = _workspaces.get(key)
     if ws is None or ws.numel() < nbytes:
-        ws = new_workspace(nbytes, device)
-        _workspaces[key] = ws
+        with torch.cuda.stream(s):
+            fresh = new_workspace(nbytes, device)
+        if ws is not None:
+            _retired.append(ws)
+        _workspaces[key] = ws = fresh
     return ws
 
 
 def release_workspaces() -> None:
-    """Drop the workspaces the binding allocated for calls made without one (one
-    per device, stream and op). Call it only when no such call is in flight on
-    the device; the next call allocates a fresh, zeroed workspace."""
+    """Free the workspaces the binding allocated for calls made without one (one
+    per device, stream and op, plus any outgrown by larger shapes). Call it only
+    when no such call is in flight, and only after dropping every CUDA graph
+    captured through such calls: a captured graph replays into the workspace
+    address it saw at capture time. The next call allocates a fresh, zeroed
+    workspace."""
     _workspaces.clear()
+    _retired.clear()
 
 
 def _layer(fn_name: str, x, qweight, scales, qzeros, group_size: int, out=None, workspace=None,
@@ -230,7 +247,7 @@ def _layer(fn_name: str, x, qweight, scales, qzeros, group_size: int, out=None, 
     if workspace is None:
         op = OP_GEMV if fn_name == "w4a16_gemv" else OP_GEMM
         need = lib.w4a16_workspace_bytes(op, M, N, K, group_size)
-        workspace = _cached_workspace(need, x.device, sp, op) if need else None
+        workspace = _cached_workspace(need, x.device, stream, op) if need else None
     ws_ptr, ws_bytes = (0, 0) if workspace is None else (workspace.data_ptr(),
                                                           workspace.numel() * workspace.element_size())
     _check(fn_name, getattr(lib, fn_name)(x.data_ptr(), qweight.data_ptr(), scales.data_ptr(), zp,
@@ -317,7 +334,7 @@ def _mx_layer(fn_name: str, x, qweight, escale, out, workspace, stream):
     if workspace is None:
         op = OP_GEMM if fn_name == "w4a16_mxfp4_gemm" else OP_GEMV
         need = lib.w4a16_workspace_bytes(op, M, N, K, 32)
-        workspace = _cached_workspace(need, x.device, sp, op) if need else None
+        workspace = _cached_workspace(need, x.device, stream, op) if need else None
     ws_ptr, ws_bytes = (0, 0) if workspace is None else (workspace.data_ptr(),
                                                           workspace.numel() * workspace.element_size())
     if fn_name == "w4a16_mxfp4_gemm":

@@ -193,9 +193,14 @@ w4a16_status w4a16_gemv_noalloc(const void* x, const int32_t* qweight, const voi
     if ((st = device_gate(&dp)) != W4A16_OK) return st;
     const w4a16::GemvPlan plan = w4a16::plan_gemv((int)M, (int)N, (int)K, (int)g, dp);
     if (w4a16::gemv_workspace_bytes(plan) > w4a16::kGemvNoAllocScratchBytes) return W4A16_ERR_WORKSPACE;
-    void* scratch = nullptr;
-    if (w4a16::gemv_noalloc_scratch(dp.device, &scratch) != cudaSuccess) return W4A16_ERR_CUDA;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // The first call on a device looks the array's address up, which must not
+    // happen inside a stream capture: refuse it there instead.
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cap) != cudaSuccess) return W4A16_ERR_CUDA;
+    void* scratch = nullptr;
+    if (w4a16::gemv_noalloc_scratch(dp.device, cap == cudaStreamCaptureStatusNone, &scratch) != cudaSuccess)
+        return W4A16_ERR_CUDA;
     // the ticket words must start at zero; the partial sums are written before they are read
     if (cudaMemsetAsync(static_cast<uint8_t*>(scratch) + plan.partial_bytes, 0, plan.ticket_bytes, s) != cudaSuccess)
         return W4A16_ERR_CUDA;

@@ -589,17 +589,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
             const int slot = c0 > 0 ? 0 : 1;
             float* part = a.partials + (static_cast<size_t>(b) * 2 + slot) * EM;
             for (int e = threadIdx.x; e < EM; e += kThreads) part[e] = red[e];
-            __threadfence();
             __syncthreads();
             const long long first = static_cast<long long>(cb) * chunks, last = first + chunks - 1;
             const int b_lo = owner_cta(first, T, Gd), b_hi = owner_cta(last, T, Gd);
+            // One acquire-release increment publishes every thread's partial (the
+            // CTA barrier above orders them before it) and, for the last
+            // contributor, makes the others' partials visible to the loads below.
             if (threadIdx.x == 0) {
-                const unsigned old = atomicAdd(a.tickets + cb, 1u);
+                unsigned old;
+                asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(a.tickets + cb) : "memory");
                 s_last = (old == static_cast<unsigned>(b_hi - b_lo));
             }
             __syncthreads();
             if (s_last) {
-                __threadfence();
                 // Contributor b_lo covers the block's first chunks, so its segment
                 // starts at chunk 0 and it wrote slot 1; every later contributor
                 // starts inside the block and wrote slot 0 (no CTA has an empty
@@ -846,12 +848,13 @@ cudaError_t launch_mx_gemv(const void* x, const uint32_t* qw, const uint8_t* es,
 // w4a16_gemv_noalloc clears them before each launch as well.
 static __device__ __align__(256) uint8_t g_gemv_noalloc_scratch[kGemvNoAllocScratchBytes];
 
-cudaError_t gemv_noalloc_scratch(int device, void** ptr) {
+cudaError_t gemv_noalloc_scratch(int device, bool may_look_up, void** ptr) {
     static std::mutex mu;
     static void* cache[64] = {nullptr};
     if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(mu);
     if (!cache[device]) {
+        if (!may_look_up) return cudaErrorStreamCaptureUnsupported;
         // host code may not use the array's name as an address: ask the runtime,
         // with `device` current (the caller's current device)
         void* p = nullptr;

@@ -33,9 +33,12 @@ struct GemvPlan {
     int cols = 0;           // columns per lane
     int cb = 0;             // columns per column block (32 * cols)
     int n_cb = 0;           // column blocks
-    int warps = 8;          // warps per CTA
+    int warps = 0;          // warps per CTA (streaming warps + one reduction warp)
     int grid = 0;           // persistent CTAs (two per SM at most)
     long long items = 0;    // column blocks x 32-row chunks of K
+    long long items_split = 0;   // items of the blocks shared stream-K by all CTAs ([0, whole_first))
+    int whole_first = 0;    // first of the blocks handed out whole
+    int whole_per_cta = 0;  // whole blocks per CTA (after its stream-K share)
     bool fact = false;      // zero-point applied per chunk through chunk sums of x
     bool xpre = false;      // with fact: the chunk sums computed once per CTA up front
     size_t smem_bytes = 0;  // dynamic shared memory per CTA
@@ -61,8 +64,10 @@ cudaError_t launch_gemv(const void* x, const uint32_t* qw, const void* sc, const
 constexpr size_t kGemvNoAllocScratchBytes = size_t(4) << 20;
 
 // Device address of that array on `device` (which must be current); looked up
-// once per device and cached.
-cudaError_t gemv_noalloc_scratch(int device, void** ptr);
+// once per device and cached. With may_look_up false (the caller's stream is
+// being captured) an address not yet cached is not looked up:
+// cudaErrorStreamCaptureUnsupported.
+cudaError_t gemv_noalloc_scratch(int device, bool may_look_up, void** ptr);
 
 cudaError_t launch_gemm(const void* x, const uint32_t* qw, const void* sc, const uint32_t* qz, void* y,
                         int M, int N, int K, int g, bool bf16, const DeviceProps& dp, cudaStream_t s);
