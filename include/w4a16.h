@@ -114,9 +114,12 @@ w4a16_status w4a16_unpack(const int32_t* src, uint8_t* dst, int64_t rows, int64_
 
 /*
  * w4a16_workspace_bytes -- bytes of device workspace `op` needs for this shape
- * on the current device. For the GEMV: a region of FP32 partial-sum slots
- * whose size depends only on the device (8 KB per SM), followed by one 32-bit
- * ticket per column block of the shape (rounded up to 256 bytes). For the GEMM
+ * on the current device. For the GEMV: the FP32 partial-sum slots of its
+ * CUDA-core kernel (8 KB per SM), then those of the few-row tensor-core kernel
+ * it runs for 5..16 rows of large layers (128 KB per SM; both sizes depend
+ * only on the device), then the ticket words of whichever kernel needs more
+ * for this shape (one per column block, or four per 128 columns; rounded up
+ * to 256 bytes). For the GEMM
  * with M <= 128: FP32 partial slots of 128 KB per SM, followed by four 32-bit
  * tickets per 128 columns (rounded up to 256 bytes); 0 for the GEMM with
  * M > 128. The same sizes serve w4a16_mxfp4_gemv and w4a16_mxfp4_gemm with
@@ -126,6 +129,15 @@ size_t w4a16_workspace_bytes(w4a16_op op, int64_t M, int64_t N, int64_t K, int64
 
 /*
  * w4a16_gemv -- decode path, 1 <= M <= 16.
+ *
+ * With M >= 5 rows and at least 8 Mi weights (N * K >= 8 * 2^20) the call
+ * runs the few-row tensor-core kernel of w4a16_gemm instead of the CUDA-core
+ * kernel described below: the CUDA-core kernel spends 8 * M FMAs on every
+ * packed word and is ALU-bound from M = 5 on (measured at N = 43008,
+ * K = 5376: 94.6 against 68.5 us at M = 5, 234 against 68.4 us at M = 16).
+ * Smaller layers stay on CUDA cores for every M. Both kernels keep their
+ * partial sums in separate regions of the workspace and share its ticket
+ * words, which every call leaves at zero.
  *
  * Streams qweight, scales and qzeros once with 128-bit coalesced loads; the
  * loads of the next 32-row chunk of K are in flight while the current one is
@@ -198,7 +210,11 @@ w4a16_status w4a16_gemv(const void* x, const int32_t* qweight, const void* scale
  *   8 KB per SM and each column block a 4-byte ticket (column blocks are 32
  *   columns wide for 9 <= M <= 16 and wider for smaller M), so on a 152-SM
  *   GB300 every N up to about 23 million columns fits.
- * Results are identical to w4a16_gemv's for the same inputs. Other errors as
+ * It always runs the CUDA-core GEMV kernel (the tensor-core kernel's scratch
+ * does not fit the array), so its results are identical to w4a16_gemv's
+ * wherever w4a16_gemv runs that kernel too: M <= 4, or fewer than 8 Mi
+ * weights; for 5..16 rows of a larger layer they agree within the parity
+ * tolerance but are slower. Other errors as
  * for w4a16_gemv.
  */
 w4a16_status w4a16_gemv_noalloc(const void* x, const int32_t* qweight, const void* scales,
@@ -210,8 +226,10 @@ w4a16_status w4a16_gemv_noalloc(const void* x, const int32_t* qweight, const voi
  *
  * M <= 128 runs an operand-swapped kernel: 128 weight columns per tile, the
  * dequantised weight tile as the MMA's 128-row operand and x (padded to 32,
- * 64 or 128 rows) as the other, so no MMA work is spent on 256-row tiles. Its
- * (column block, 64-deep K step) pairs are split into equal contiguous ranges,
+ * 64 or 128 rows) as the other, so no MMA work is spent on 256-row tiles. The
+ * dequantised tile is written straight into tensor memory and the MMA reads
+ * it there. Its (column block, K step) pairs (256 deep up to 64 padded rows of
+ * x, 128 above) are split into equal contiguous ranges,
  * one per SM (stream-K); a column block split between CTAs is finished by the
  * last of them, which sums their FP32 partials from the workspace in
  * ascending CTA order (deterministic). This path needs a workspace of
@@ -295,9 +313,10 @@ w4a16_status w4a16_mxfp4_dequant(const int32_t* qweight, const uint8_t* escale, 
  * w4a16_gemv kernel with the E2M1 decode in place of the 4-bit integer one
  * (each 32-row chunk is one exponent block; its scale 2^(e - 127) is applied
  * in FP32 once per chunk). Same persistent grid, deterministic fix-up and
- * programmatic launch. Workspace: at least w4a16_workspace_bytes(W4A16_OP_GEMV,
- * M, N, K, 32) bytes, with the same ownership and zero-fill rules as for
- * w4a16_gemv.
+ * programmatic launch; like w4a16_gemv, 5..16 rows of a layer with at least
+ * 8 Mi weights run the few-row tensor-core kernel of w4a16_mxfp4_gemm instead.
+ * Workspace: at least w4a16_workspace_bytes(W4A16_OP_GEMV, M, N, K, 32) bytes,
+ * with the same ownership and zero-fill rules as for w4a16_gemv.
  */
 w4a16_status w4a16_mxfp4_gemv(const void* x, const int32_t* qweight, const uint8_t* escale, void* y, int64_t M,
                               int64_t N, int64_t K, void* workspace, size_t workspace_bytes,

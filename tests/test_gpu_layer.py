@@ -218,7 +218,7 @@ def test_gemm_stream_k_workspace_reuse():
 
 def test_gemv_workspace_reuse_across_shapes():
     """One workspace serves calls of different shapes: every call leaves its tickets at zero."""
-    ws = w4.new_workspace(8 << 20)
+    ws = w4.new_workspace(32 << 20)
     cases = [DeviceCase(make_case(M, N, K, 32, "f16", False, seed=M + N))
              for (M, N, K) in ((1, 4104, 2048), (3, 1032, 4096), (1, 43008, 512), (7, 264, 256))]
     for _ in range(2):
@@ -227,6 +227,21 @@ def test_gemv_workspace_reuse_across_shapes():
             assert 0 < need <= ws.numel()
             y = w4.gemv(dc.x, dc.qw, dc.s, dc.qz, 32, workspace=ws)
             assert_within_tol(y, dc.reference(), "f16", "reuse")
+
+
+def test_gemv_workspace_shared_by_both_kernels():
+    """Calls that run the CUDA-core GEMV and calls that run the few-row
+    tensor-core kernel, alternating on one workspace: partial sums of either
+    never land on the ticket words the other relies on."""
+    cases = [DeviceCase(make_case(M, N, K, 32, "bf16", False, seed=M + N))
+             for (M, N, K) in ((16, 8192, 1024), (1, 4104, 2048), (8, 43008, 256), (3, 1032, 4096))]
+    need = max(w4.workspace_bytes(w4.OP_GEMV, dc.case.M, dc.case.N, dc.case.K, 32) for dc in cases)
+    ws = w4.new_workspace(need)
+    for _ in range(3):
+        for dc in cases:
+            y = w4.gemv(dc.x, dc.qw, dc.s, dc.qz, 32, workspace=ws)
+            assert_within_tol(y, dc.reference(), "bf16", f"shared workspace M={dc.case.M} N={dc.case.N}")
+    assert w4.device_status() == w4.OK
 
 
 def test_gemv_workspace_too_small():
@@ -256,3 +271,22 @@ def test_binding_rejections():
     with pytest.raises(w4.W4A16Error) as e:
         w4.gemv(x17, dc.qw, dc.s, dc.qz, 32)
     assert e.value.status == w4.ERR_SHAPE
+
+
+@pytest.mark.parametrize("M,N,K,g,act", [(5, 4104, 2048, 32, "f16"), (8, 8192, 1024, 128, "bf16"),
+                                         (16, 2056, 4096, 64, "f16"), (12, 43008, 256, 32, "bf16")])
+def test_gemv_tensor_core_rows(M, N, K, g, act):
+    """w4a16_gemv hands 5..16 rows of a layer with at least 8 Mi weights to the
+    few-row tensor-core kernel (workspace sized by w4a16_workspace_bytes for
+    the GEMV): parity with the oracle, and two calls bit-identical."""
+    assert N * K >= 8 << 20
+    dc = DeviceCase(make_case(M, N, K, g, act, False, seed=M * 3 + g))
+    need = w4.workspace_bytes(w4.OP_GEMV, M, N, K, g)
+    assert need > w4.workspace_bytes(w4.OP_GEMM, M, N, K, g)   # both kernels' partial regions
+    ws = w4.new_workspace(need)
+    y1 = w4.gemv(dc.x, dc.qw, dc.s, dc.qz, g, workspace=ws)
+    y2 = w4.gemv(dc.x, dc.qw, dc.s, dc.qz, g, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2)
+    assert_within_tol(y1, dc.reference(), act, f"gemv {M}x{N}x{K} g{g} (tensor cores)")
+    assert w4.device_status() == w4.OK

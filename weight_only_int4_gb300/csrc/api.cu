@@ -166,7 +166,7 @@ size_t w4a16_workspace_bytes(w4a16_op op, int64_t M, int64_t N, int64_t K, int64
     DeviceProps dp;
     if (device_gate(&dp) != W4A16_OK) return 0;
     if (op == W4A16_OP_GEMM) return w4a16::skinny_workspace_bytes((int)N, dp);
-    return w4a16::gemv_workspace_bytes(w4a16::plan_gemv((int)M, (int)N, (int)K, (int)g, dp));
+    return w4a16::gemv_workspace(w4a16::plan_gemv((int)M, (int)N, (int)K, (int)g, dp), (int)N, dp).total();
 }
 
 w4a16_status w4a16_gemv(const void* x, const int32_t* qweight, const void* scales, const int32_t* qzeros, void* y,
@@ -178,10 +178,20 @@ w4a16_status w4a16_gemv(const void* x, const int32_t* qweight, const void* scale
     DeviceProps dp;
     if ((st = device_gate(&dp)) != W4A16_OK) return st;
     const w4a16::GemvPlan plan = w4a16::plan_gemv((int)M, (int)N, (int)K, (int)g, dp);
-    if (workspace_bytes < w4a16::gemv_workspace_bytes(plan)) return W4A16_ERR_WORKSPACE;
+    const w4a16::GemvWorkspace wl = w4a16::gemv_workspace(plan, (int)N, dp);
+    if (workspace_bytes < wl.total()) return W4A16_ERR_WORKSPACE;
+    if (w4a16::gemv_uses_tensor_cores(M, N, K)) {
+        // 5..16 rows of a large layer: the few-row tensor-core kernel is faster
+        return from_cuda(w4a16::launch_gemm_skinny(x, reinterpret_cast<const uint32_t*>(qweight), scales,
+                                                   reinterpret_cast<const uint32_t*>(qzeros), y, (int)M, (int)N,
+                                                   (int)K, (int)g, dt == W4A16_BF16, wl.tensor_part(workspace),
+                                                   wl.ticket_words(workspace), dp,
+                                                   reinterpret_cast<cudaStream_t>(stream)));
+    }
     return from_cuda(w4a16::launch_gemv(x, reinterpret_cast<const uint32_t*>(qweight), scales,
                                         reinterpret_cast<const uint32_t*>(qzeros), y, (int)M, (int)N, (int)K, (int)g,
-                                        dt == W4A16_BF16, plan, workspace, reinterpret_cast<cudaStream_t>(stream)));
+                                        dt == W4A16_BF16, plan, wl.cuda_part(workspace), wl.ticket_words(workspace),
+                                        reinterpret_cast<cudaStream_t>(stream)));
 }
 
 w4a16_status w4a16_gemv_noalloc(const void* x, const int32_t* qweight, const void* scales, const int32_t* qzeros,
@@ -206,7 +216,9 @@ w4a16_status w4a16_gemv_noalloc(const void* x, const int32_t* qweight, const voi
         return W4A16_ERR_CUDA;
     return from_cuda(w4a16::launch_gemv(x, reinterpret_cast<const uint32_t*>(qweight), scales,
                                         reinterpret_cast<const uint32_t*>(qzeros), y, (int)M, (int)N, (int)K, (int)g,
-                                        dt == W4A16_BF16, plan, scratch, s));
+                                        dt == W4A16_BF16, plan, static_cast<float*>(scratch),
+                                        reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(scratch) + plan.partial_bytes),
+                                        s));
 }
 
 w4a16_status w4a16_gemm(const void* x, const int32_t* qweight, const void* scales, const int32_t* qzeros, void* y,
@@ -219,10 +231,11 @@ w4a16_status w4a16_gemm(const void* x, const int32_t* qweight, const void* scale
     if ((st = device_gate(&dp)) != W4A16_OK) return st;
     if (M <= w4a16::kSkinnyMaxM) {
         if (workspace_bytes < w4a16::skinny_workspace_bytes((int)N, dp)) return W4A16_ERR_WORKSPACE;
-        return from_cuda(w4a16::launch_gemm_skinny(x, reinterpret_cast<const uint32_t*>(qweight), scales,
-                                                   reinterpret_cast<const uint32_t*>(qzeros), y, (int)M, (int)N,
-                                                   (int)K, (int)g, dt == W4A16_BF16, workspace, dp,
-                                                   reinterpret_cast<cudaStream_t>(stream)));
+        return from_cuda(w4a16::launch_gemm_skinny(
+            x, reinterpret_cast<const uint32_t*>(qweight), scales, reinterpret_cast<const uint32_t*>(qzeros), y,
+            (int)M, (int)N, (int)K, (int)g, dt == W4A16_BF16, static_cast<float*>(workspace),
+            reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(workspace) + w4a16::skinny_partial_bytes(dp)), dp,
+            reinterpret_cast<cudaStream_t>(stream)));
     }
     return from_cuda(w4a16::launch_gemm(x, reinterpret_cast<const uint32_t*>(qweight), scales,
                                         reinterpret_cast<const uint32_t*>(qzeros), y, (int)M, (int)N, (int)K, (int)g,
@@ -277,9 +290,16 @@ w4a16_status w4a16_mxfp4_gemv(const void* x, const int32_t* qweight, const uint8
     DeviceProps dp;
     if ((st = device_gate(&dp)) != W4A16_OK) return st;
     const w4a16::GemvPlan plan = w4a16::plan_mx_gemv((int)M, (int)N, (int)K, dp);
-    if (workspace_bytes < w4a16::gemv_workspace_bytes(plan)) return W4A16_ERR_WORKSPACE;
+    const w4a16::GemvWorkspace wl = w4a16::gemv_workspace(plan, (int)N, dp);
+    if (workspace_bytes < wl.total()) return W4A16_ERR_WORKSPACE;
+    if (w4a16::gemv_uses_tensor_cores(M, N, K))
+        return from_cuda(w4a16::launch_mx_gemm_skinny(x, reinterpret_cast<const uint32_t*>(qweight), escale, y, (int)M,
+                                                      (int)N, (int)K, wl.tensor_part(workspace),
+                                                      wl.ticket_words(workspace), dp,
+                                                      reinterpret_cast<cudaStream_t>(stream)));
     return from_cuda(w4a16::launch_mx_gemv(x, reinterpret_cast<const uint32_t*>(qweight), escale, y, (int)M, (int)N,
-                                           (int)K, plan, workspace, reinterpret_cast<cudaStream_t>(stream)));
+                                           (int)K, plan, wl.cuda_part(workspace), wl.ticket_words(workspace),
+                                           reinterpret_cast<cudaStream_t>(stream)));
 }
 
 w4a16_status w4a16_mxfp4_gemm(const void* x, const int32_t* qweight, const uint8_t* escale, void* y, int64_t M,
@@ -293,7 +313,9 @@ w4a16_status w4a16_mxfp4_gemm(const void* x, const int32_t* qweight, const uint8
     const uint32_t* qw = reinterpret_cast<const uint32_t*>(qweight);
     if (M <= w4a16::kSkinnyMaxM) {
         if (workspace_bytes < w4a16::skinny_workspace_bytes((int)N, dp)) return W4A16_ERR_WORKSPACE;
-        return from_cuda(w4a16::launch_mx_gemm_skinny(x, qw, escale, y, (int)M, (int)N, (int)K, workspace, dp, s));
+        return from_cuda(w4a16::launch_mx_gemm_skinny(
+            x, qw, escale, y, (int)M, (int)N, (int)K, static_cast<float*>(workspace),
+            reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(workspace) + w4a16::skinny_partial_bytes(dp)), dp, s));
     }
     return from_cuda(w4a16::launch_mx_gemm(x, qw, escale, y, (int)M, (int)N, (int)K, dp, s));
 }

@@ -4,14 +4,20 @@
 // For small M the weights dominate everything: the layer must stream and
 // dequantise K*N weights whatever M is, while the MMA work shrinks with M.
 // Here the unit of work is a 128-column block of weights with all M rows:
-// the dequantised weight tile [128 x 64] is the MMA's A operand (M_mma = 128),
-// the x tile [MP x 64] its B operand (N_mma = MP, M rounded up to a multiple
-// of 32), and each CTA's tensor memory holds D[n][m] = y[m][n] for its
-// columns. The weight tile is loaded and dequantised once per CTA and every
-// row of x reuses it (the cooperative shared tile of "ROCm
+// the dequantised weight tile [128 x 128] is the MMA's A operand (M_mma =
+// 128), the x tile [MP x 128] its B operand (N_mma = MP, M rounded up to a
+// multiple of 32), and each CTA's tensor memory holds D[n][m] = y[m][n] for
+// its columns. The weight tile is loaded and dequantised once per CTA and
+// every row of x reuses it (the cooperative shared tile of "ROCm
 // KQuantGemmKWmmaQ4K/Q6K: redesign around a cooperative shared tile",
-// section "Confirmed mechanism"), as in the prefill GEMM, but no tile is
-// padded to 256 rows of x.
+// section "Confirmed mechanism"), but the shared tile lives in tensor memory:
+// the dequantising threads write it there with tcgen05.st (thread = weight
+// column = tensor-memory lane) and the MMA reads A from tensor memory. No
+// shared-memory operand ring, no swizzled stores; tensor memory holds two
+// accumulators and four to six operand stages, shared memory only the load
+// ring. A tcgen05.mma with M = 128, K = 16 takes about 93 cycles for any N up
+// to 128 (measured on GB300), so the MMA count per weight, not the rows of x,
+// sets this kernel's floor: about 33 us at 43008 x 5376.
 //
 // Work is split stream-K: the (column block, K step) pairs, column block
 // first, are cut into equal contiguous ranges, one per CTA (one CTA per SM),
@@ -26,17 +32,18 @@
 //
 // Warp roles, one CTA per SM, each walking the CTA's (column block, K range)
 // segments in order:
-//   warp 0      producer: per K step (128 deep for up to 64 padded rows of x,
-//               else 64), TMA brings the x tile [MP x step] in 64-column
+//   warp 0      producer: per 128-deep K step, TMA brings the x tile [MP x 128] in 64-column
 //               boxes (128-byte swizzle, rows >= M zero-filled) and the packed
 //               weight tile [step/8 words x 128]; the lanes stage the step's
 //               scales and zero-point words with cp.async. One mbarrier per stage.
 //   warps 8-23  two groups of eight on alternate K steps dequantise the packed
-//               tile into the canonical K-major 128-byte-swizzled operand tile
-//               (one or two 64-deep sub-tiles): w = (q - z) * s, (q - z) exact
-//               in 16-bit arithmetic, one rounding.
-//   warp 1      one thread issues step/16 x tcgen05.mma (kind::f16, M=128,
-//               N=MP, K=16) per step into one of two MP-column FP32 accumulators.
+//               tile into an operand stage of tensor memory: warp w writes
+//               lanes 32 (w % 4) .. + 31 (its quarter), the two warps of a
+//               quarter the two 64-deep halves of the step; w = (q - z) * s,
+//               (q - z) exact in 16-bit arithmetic, one rounding.
+//   warp 1      one thread issues 8 x tcgen05.mma (kind::f16, M=128, N=MP,
+//               K=16, A from tensor memory) per step into one of two
+//               MP-column FP32 accumulators.
 //   warps 4-7   epilogue: tcgen05.ld of the accumulator (lane = column n,
 //               column = row m of x), round, store y[m][n] (consecutive lanes
 //               write consecutive columns), predicated on m < M and n < N.
@@ -52,6 +59,7 @@
 #include "tmap.h"
 
 #include <algorithm>
+#include <cstring>
 
 namespace w4a16 {
 
@@ -59,20 +67,17 @@ __device__ unsigned int g_skinny_error = 0;
 
 namespace {
 
-// Row buckets up to this many padded rows of x take 128-deep K steps (twice the
-// work per pipeline hand-off); larger ones 64-deep steps, which leave room for
-// more load stages. Measured at N = 43008, K = 5376: 128-deep steps 6-10 %
-// faster for M <= 64, twice as slow at MP = 128 (two load stages).
-#ifndef W4A16_SKINNY_BK128_MAX_MP
-#define W4A16_SKINNY_BK128_MAX_MP 64
-#endif
 constexpr int BN = 128;                  // weight columns per tile (M of the MMA)
 constexpr int kThreads = 768;
 constexpr int kEpiWarp0 = 4;             // warps 4..7
-constexpr int kDeqWarp0 = 8;             // warps 8..23: two groups taking alternate K steps
-constexpr int kDeqWarps = 8;
-constexpr int kDeqGroups = 2;
-constexpr uint32_t kSubBytes = BN * 64 * 2;          // 16 KB: one 64-deep sub-tile of the operand
+constexpr int kDeqWarp0 = 8;             // warps 8..23: groups taking K steps in turn
+#ifndef W4A16_SKINNY_DEQ_GROUPS
+#define W4A16_SKINNY_DEQ_GROUPS 2
+#endif
+constexpr int kDeqGroups = W4A16_SKINNY_DEQ_GROUPS;   // 2 or 4
+constexpr int kDeqWarps = 16 / kDeqGroups;            // warps per group: every quarter of the lanes, once or twice
+constexpr int kDeqSplit = kDeqWarps / 4;              // threads per weight column in a group
+constexpr uint32_t kTmemCols = 512;      // the whole tensor memory of the SM (one CTA per SM)
 constexpr uint32_t kSuspendNs = 20000;
 constexpr unsigned long long kWaitLimitCycles = 4000000000ull;   // ~2 s at 2 GHz
 constexpr unsigned int kErrTimeout = 9u;
@@ -80,28 +85,31 @@ constexpr size_t kSmemBudget = 220 * 1024;
 
 template <int MP>
 struct Cfg {
-    static_assert(MP % 32 == 0 && MP >= 32 && MP <= 256, "rows of x per tile");
-    static constexpr int BK = MP <= W4A16_SKINNY_BK128_MAX_MP ? 128 : 64;   // K per step
-    static constexpr int kSub = BK / 64;            // 64-deep sub-tiles per step (one 128-byte swizzle row each)
+    static_assert(MP % 32 == 0 && MP >= 32 && MP <= 128, "rows of x per tile");
+    // K per step: 256 up to 64 padded rows of x (half the per-step pipeline
+    // hand-offs: 68-75 us against 71-81 us with 128 at N = 43008, K = 5376);
+    // 128 above, where a 256-deep step leaves room for only two load stages
+    static constexpr int BK = MP <= 64 ? 256 : 128;
+    static constexpr int kSub = BK / 64;            // 64-column boxes of x per step (one 128-byte swizzle row each)
     static constexpr int kQuarters = BK / 32;       // 32-row scale blocks per step
-#ifndef W4A16_SKINNY_BK128_B_STAGES
-#define W4A16_SKINNY_BK128_B_STAGES 2
-#endif
-    static constexpr int kBStages = BK == 128 ? W4A16_SKINNY_BK128_B_STAGES : 4;
     static constexpr uint32_t kWBytes = (BK / 8) * BN * 4;          // packed weights
     static constexpr uint32_t kSBytes = kQuarters * BN * 2;         // scales of the step's 32-row blocks
     static constexpr uint32_t kZBytes = kQuarters * (BN / 8) * 4;   // zero-point words of the blocks
-    static constexpr uint32_t kBBytes = kSub * kSubBytes;           // dequantised operand tile
-    static constexpr uint32_t kABytes = MP * BK * 2;                                   // x tile
+    static constexpr uint32_t kABytes = MP * BK * 2;                // x tile
     static constexpr uint32_t kLoadStageBytes = (kABytes + kWBytes + kSBytes + kZBytes + 1023) & ~1023u;
-    // as many load stages as fit beside the operand ring, an even number (each
-    // dequant group then owns whole load stages: no waiter skips a phase)
-    static constexpr int kRaw = static_cast<int>((kSmemBudget - 2048 - kBStages * kBBytes) / kLoadStageBytes);
-    static constexpr int kLoadStages = (kRaw > 10 ? 10 : kRaw) & ~1;
-    static constexpr uint32_t kAccCols = MP;              // one accumulator
-    static constexpr uint32_t kTmemCols = 2 * MP < 32 ? 32 : 2 * MP;   // two accumulators, power of two
-    static_assert(kLoadStages >= 2, "load ring");
-    static_assert(kLoadStages % kDeqGroups == 0 && kBStages % kDeqGroups == 0,
+    // as many load stages as fit (at most 10), a multiple of the dequant groups
+    // (each group then owns whole ring stages: no waiter skips a phase)
+    static constexpr int kRaw = static_cast<int>((kSmemBudget - 2048) / kLoadStageBytes);
+    static constexpr int kLoadStages = (kRaw > 10 ? 10 : kRaw) & ~(kDeqGroups - 1);
+    // tensor memory: two accumulators of MP columns, then operand stages of
+    // BK / 2 columns (two 16-bit values per 32-bit column), a multiple of the groups
+    static constexpr uint32_t kAccCols = MP;
+    static constexpr uint32_t kOpCol0 = 2 * MP;
+    static constexpr uint32_t kOpCols = BK / 2;
+    static constexpr int kOpStages = static_cast<int>((kTmemCols - kOpCol0) / kOpCols) & ~(kDeqGroups - 1);
+    static_assert(kLoadStages >= 2 && kOpStages >= 2, "rings");
+    static_assert(kLoadStages % 2 == 0, "two producer warps own alternate load stages");
+    static_assert(kLoadStages % kDeqGroups == 0 && kOpStages % kDeqGroups == 0,
                   "each dequant group owns whole ring stages");
 };
 
@@ -109,8 +117,8 @@ template <int MP>
 struct __align__(8) Barriers {
     uint64_t lfull[Cfg<MP>::kLoadStages];
     uint64_t lempty[Cfg<MP>::kLoadStages];
-    uint64_t bfull[Cfg<MP>::kBStages];
-    uint64_t bempty[Cfg<MP>::kBStages];
+    uint64_t afull[Cfg<MP>::kOpStages];    // operand stage written (tensor memory)
+    uint64_t aempty[Cfg<MP>::kOpStages];   // operand stage read by the MMAs
     uint64_t tfull[2];
     uint64_t tempty[2];
     uint64_t drain;
@@ -120,11 +128,16 @@ struct __align__(8) Barriers {
 
 template <int MP>
 constexpr size_t smem_bytes() {
-    return 1024 + Cfg<MP>::kLoadStages * Cfg<MP>::kLoadStageBytes + Cfg<MP>::kBStages * Cfg<MP>::kBBytes +
-           sizeof(Barriers<MP>);
+    return 1024 + Cfg<MP>::kLoadStages * Cfg<MP>::kLoadStageBytes + sizeof(Barriers<MP>);
 }
 
+#ifndef W4A16_SKINNY_SPIN
+#define W4A16_SKINNY_SPIN 64
+#endif
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort) {
+    // a completed or nearly completed phase is seen without the suspend path's cost
+    for (int i = 0; i < W4A16_SKINNY_SPIN; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = clock64();
     for (;;) {
         if (mbar_try_wait_suspend(bar, parity, kSuspendNs)) return true;
@@ -219,29 +232,28 @@ struct Dq<true> {
 template <bool kBf16, bool kSym, int MP, bool kMx = false>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
-                   const uint16_t* __restrict__ sc, const uint32_t* __restrict__ qz, uint16_t* __restrict__ y, int M,
-                   int N, int K, int g, float* __restrict__ partials, uint32_t* __restrict__ tickets, int streamk) {
+                   const __grid_constant__ CUtensorMap tmap_s, const __grid_constant__ CUtensorMap tmap_z,
+                   const uint32_t* __restrict__ qz, uint16_t* __restrict__ y, int M, int N, int K, int g,
+                   float* __restrict__ partials, uint32_t* __restrict__ tickets, int streamk, int z_tma) {
     using C = Cfg<MP>;
     constexpr int L = C::kLoadStages;
-    constexpr int BK = C::BK, kSub = C::kSub, kBStages = C::kBStages;
-    constexpr uint32_t kWBytes = C::kWBytes, kSBytes = C::kSBytes, kBBytes = C::kBBytes;
+    constexpr int BK = C::BK, kSub = C::kSub, kOpStages = C::kOpStages;
+    constexpr uint32_t kWBytes = C::kWBytes, kSBytes = C::kSBytes;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* bsmem = smem + L * C::kLoadStageBytes;
-    Barriers<MP>* bars = reinterpret_cast<Barriers<MP>*>(bsmem + kBStages * kBBytes);
+    Barriers<MP>* bars = reinterpret_cast<Barriers<MP>*>(smem + L * C::kLoadStageBytes);
     const uint32_t smem_base = smem_u32(smem);
-    const uint32_t bsmem_base = smem_u32(bsmem);
     // load stage s: [x tile | packed weights | scales | zero-point words]
     auto ld_a = [&](int s) { return smem_base + s * C::kLoadStageBytes; };
     auto ld_w = [&](int s) { return smem + s * C::kLoadStageBytes + C::kABytes; };
     auto ld_s = [&](int s) { return smem + s * C::kLoadStageBytes + C::kABytes + kWBytes; };
     auto ld_z = [&](int s) { return smem + s * C::kLoadStageBytes + C::kABytes + kWBytes + kSBytes; };
-    auto op_w = [&](int s) { return bsmem_base + s * kBBytes; };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tiles = (N + BN - 1) / BN;
     const int kt_total = (K + BK - 1) / BK;
     const int groups = K / g;
+    const int srows = g <= BK ? BK / g : 1;   // scale / zero-point rows per K step
     volatile int* abort_flag = &bars->abort;
     const long long U = static_cast<long long>(tiles) * kt_total;
     const int G = gridDim.x;
@@ -253,9 +265,9 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_cons
             mbar_init(smem_u32(&bars->lfull[s]), 1);
             mbar_init(smem_u32(&bars->lempty[s]), 1);
         }
-        for (int s = 0; s < kBStages; ++s) {
-            mbar_init(smem_u32(&bars->bfull[s]), kDeqWarps);
-            mbar_init(smem_u32(&bars->bempty[s]), 1);
+        for (int s = 0; s < kOpStages; ++s) {
+            mbar_init(smem_u32(&bars->afull[s]), kDeqWarps);
+            mbar_init(smem_u32(&bars->aempty[s]), 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(smem_u32(&bars->tfull[a]), 1);
@@ -266,18 +278,25 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_cons
         fence_mbar_init();
         tma_prefetch_desc(&tmap_x);
         tma_prefetch_desc(&tmap_w);
+        tma_prefetch_desc(&tmap_s);
+        if (z_tma) tma_prefetch_desc(&tmap_z);
     }
-    if (warp == 2) tmem_alloc(smem_u32(&bars->tmem_base), C::kTmemCols);
+    if (warp == 2) tmem_alloc(smem_u32(&bars->tmem_base), kTmemCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = bars->tmem_base;
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ producer warp
+    if (warp == 0 || warp == 3) {
+        // ------------------------------------------------------------ producer warps
+        // warp 0 loads the even steps, warp 3 the odd ones (one thread issuing
+        // every copy of every step could not keep up with the MMAs)
+        const int pw = warp == 0 ? 0 : 1;
         const int half = lane >> 4, sub = lane & 15;
+        (void)half;
         int stage = 0;
         uint32_t phase = 0;
+        int pj = 0;
         uint32_t issued_parity[L];
         bool issued[L];
         for (int s = 0; s < L; ++s) issued[s] = false, issued_parity[s] = 0;
@@ -288,33 +307,37 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_cons
             const int n0 = t * BN;
             const int n = n0 + 8 * sub;
             for (int kt = k0; kt < k1; ++kt) {
+                if ((pj++ & 1) != pw) {   // the other producer's step
+                    if (++stage == L) { stage = 0; phase ^= 1u; }
+                    continue;
+                }
                 if (!warp_wait_bar(smem_u32(&bars->lempty[stage]), phase ^ 1u, abort_flag, lane)) { ok = false; break; }
                 const uint32_t fb = smem_u32(&bars->lfull[stage]);
-#pragma unroll
-                for (int p = 0; p < kSub; ++p) {
-                    const int qt = 2 * p + half;                 // 32-row block of the step
-                    const int grp = (kt * BK + qt * 32) / g;
-                    const bool valid = n < N && grp < groups;
-                    const size_t so = valid ? static_cast<size_t>(grp) * N + n : 0;
-                    if constexpr (kMx) {
-                        cp_async_8(smem_u32(ld_s(stage)) + qt * BN + 8 * sub, reinterpret_cast<const uint8_t*>(sc) + so,
-                                   valid ? 8u : 0u);
-                    } else {
-                        cp_async_16(smem_u32(ld_s(stage)) + qt * (BN * 2) + 16 * sub, sc + so, valid ? 16u : 0u);
-                    }
-                    if constexpr (!kSym) {
-                        const size_t zo = valid ? static_cast<size_t>(grp) * (N >> 3) + (n >> 3) : 0;
-                        cp_async_4(smem_u32(ld_z(stage)) + qt * (BN / 8) * 4 + 4 * sub, qz + zo, valid ? 4u : 0u);
+                const int row0 = (kt * BK) / g;             // first scale / zero-point row of the step
+                if constexpr (!kSym) {
+                    if (!z_tma) {
+                        // zero-point rows of N / 8 words that are not a multiple of 16 bytes:
+                        // 4-byte copies by the lanes (rows >= K / g and columns >= N read as 0)
+                        for (int r = half; r < srows; r += 2) {
+                            const int grp = row0 + r;
+                            const bool valid = n < N && grp < groups;
+                            const size_t zo = valid ? static_cast<size_t>(grp) * (N >> 3) + (n >> 3) : 0;
+                            cp_async_4(smem_u32(ld_z(stage)) + r * (BN / 8) * 4 + 4 * sub, qz + zo, valid ? 4u : 0u);
+                        }
+                        cp_async_mbar_arrive(fb);
                     }
                 }
-                cp_async_mbar_arrive(fb);
                 __syncwarp();
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(fb, C::kABytes + kWBytes);
+                    const uint32_t ztx = (!kSym && z_tma) ? srows * (BN / 8) * 4 : 0u;
+                    mbar_arrive_expect_tx(fb, C::kABytes + kWBytes + srows * BN * (kMx ? 1 : 2) + ztx);
 #pragma unroll
                     for (int p = 0; p < kSub; ++p)   // x in 64-column boxes (the 128-byte swizzle's width)
                         tma_load_2d(ld_a(stage) + p * (MP * 128), &tmap_x, kt * BK + 64 * p, 0, fb);
                     tma_load_2d(smem_u32(ld_w(stage)), &tmap_w, n0, kt * (BK / 8), fb);
+                    // the step's scale rows (box of srows rows; rows past K / g and columns past N read as 0)
+                    tma_load_2d(smem_u32(ld_s(stage)), &tmap_s, n0, row0, fb);
+                    if (ztx) tma_load_2d(smem_u32(ld_z(stage)), &tmap_z, n0 / 8, row0, fb);
                 }
                 issued[stage] = true;
                 issued_parity[stage] = phase;
@@ -335,8 +358,8 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_cons
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t kIdesc = umma_idesc_f16(BN, MP, kBf16);
-            int ls = 0, bs = 0;
-            uint32_t bph = 0;
+            int ls = 0, as = 0;
+            uint32_t aph = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
@@ -347,22 +370,23 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_cons
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * C::kAccCols);
                 for (int kt = k0; kt < k1; ++kt) {
-                    // completes when the dequant group has written the operand tile,
+                    // completes when the dequant group has written the operand stage,
                     // which it starts only after the step's x tile has landed
-                    if (!wait_bar(smem_u32(&bars->bfull[bs]), bph, abort_flag)) { ok = false; break; }
+                    if (!wait_bar(smem_u32(&bars->afull[as]), aph, abort_flag)) { ok = false; break; }
                     tc_fence_after();
+                    const uint32_t a_tmem = tmem_base + C::kOpCol0 + static_cast<uint32_t>(as) * C::kOpCols;
 #pragma unroll
                     for (int p = 0; p < kSub; ++p) {
-                        const uint64_t wdesc = sw128_kmajor_desc(op_w(bs) + p * kSubBytes);
                         const uint64_t xdesc = sw128_kmajor_desc(ld_a(ls) + p * (MP * 128));
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            umma_f16(d_tmem, wdesc + 2u * kk, xdesc + 2u * kk, kIdesc, (kt - k0) + p + kk != 0);
+                        for (int kk = 0; kk < 4; ++kk)   // 16 values of K = 8 columns of the operand
+                            umma_f16_ta(d_tmem, a_tmem + 8u * (4 * p + kk), xdesc + 2u * kk, kIdesc,
+                                        (kt - k0) + p + kk != 0);
                     }
                     umma_commit(smem_u32(&bars->lempty[ls]));
-                    umma_commit(smem_u32(&bars->bempty[bs]));
+                    umma_commit(smem_u32(&bars->aempty[as]));
                     if (++ls == L) ls = 0;
-                    if (++bs == kBStages) { bs = 0; bph ^= 1u; }
+                    if (++as == kOpStages) { as = 0; aph ^= 1u; }
                 }
                 if (!ok) break;
                 umma_commit(smem_u32(&bars->tfull[acc]));
@@ -466,18 +490,20 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_cons
     } else if (warp >= kDeqWarp0) {
         // ------------------------------------------------------------ dequantisers
         const int tg = threadIdx.x - kDeqWarp0 * 32;    // 0..511
-        const int grp = tg >> 8;                         // group: steps j with j % kDeqGroups == grp
-        const int td = tg & 255;
-        const int d = td & (BN - 1);                     // column of the tile
-        const int tq = td >> 7;                          // this thread's 32-row blocks: kSub * tq .. kSub * tq + kSub - 1
-        int ls = 0, bs = 0;
-        uint32_t lph = 0, bph = 0;
+        const int grp = tg / (kDeqWarps * 32);           // group: steps j with j % kDeqGroups == grp
+        const int td = tg % (kDeqWarps * 32);
+        const int d = td & (BN - 1);                     // column of the tile = tensor-memory lane (warp's quarter)
+        const int tq = td >> 7;                          // this thread's part of the step's K
+        constexpr int kBlocks = C::kQuarters / kDeqSplit;   // 32-row blocks per thread
+        const uint32_t lane_field = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        int ls = 0, as = 0;
+        uint32_t lph = 0, aph = 0;
         bool ok = true;
         int j = 0;
         auto advance = [&]() {
             ++j;
             if (++ls == L) { ls = 0; lph ^= 1u; }
-            if (++bs == kBStages) { bs = 0; bph ^= 1u; }
+            if (++as == kOpStages) { as = 0; aph ^= 1u; }
         };
         Segments seg{u_begin, u_end, kt_total, streamk != 0, tiles};
         int t, k0, k1;
@@ -488,51 +514,58 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_cons
                     continue;
                 }
                 if (!warp_wait_bar(smem_u32(&bars->lfull[ls]), lph, abort_flag, lane) ||
-                    !warp_wait_bar(smem_u32(&bars->bempty[bs]), bph ^ 1u, abort_flag, lane)) {
+                    !warp_wait_bar(smem_u32(&bars->aempty[as]), aph ^ 1u, abort_flag, lane)) {
                     ok = false;
                     break;
                 }
+                tc_fence_after();   // the MMAs that read this operand stage have completed
                 const uint32_t* wt = reinterpret_cast<const uint32_t*>(ld_w(ls));
                 const uint16_t* st = reinterpret_cast<const uint16_t*>(ld_s(ls));
                 const uint32_t* zt = reinterpret_cast<const uint32_t*>(ld_z(ls));
+                const uint32_t op = tmem_base + lane_field + C::kOpCol0 + static_cast<uint32_t>(as) * C::kOpCols;
+                // this column's values of K, two 32-row blocks (32 bf16/fp16 pairs, pair c
+                // holding k = 2c, 2c + 1) per tensor-memory store
 #pragma unroll
-                for (int r = 0; r < kSub; ++r) {
-                    const int qt = tq * kSub + r;                // 32-row block: word rows 4*qt .. 4*qt+3
-                    const int p = qt >> 1, half = qt & 1;        // sub-tile, and half of its 64 rows
-                    const uint32_t* wp = wt + p * 8 * BN;        // the sub-tile's 8 word rows
-                    const uint32_t b_row = op_w(bs) + p * kSubBytes + static_cast<uint32_t>(d) * 128u;
-                    if constexpr (kMx) {
-                        mx::operand_column<BN>(wp, b_row, d, half, reinterpret_cast<const uint8_t*>(st)[qt * BN + d]);
-                        continue;
-                    }
-                    const uint32_t s16 = st[qt * BN + d];
-                    const uint32_t z4 = kSym ? 8u : ((zt[qt * (BN / 8) + (d >> 3)] >> (4 * (d & 7))) & 0xFu);
-                    const uint32_t ss = s16 | (s16 << 16);
-                    const uint32_t zz = Dq<kBf16>::kMagic | z4 | (z4 << 16);
+                for (int r2 = 0; r2 < kBlocks; r2 += 2) {
+                    uint32_t o[32];
 #pragma unroll
-                    for (int cc = 0; cc < 4; ++cc) {
-                        const int c = half * 4 + cc;
-                        const uint32_t w = wp[c * BN + d];
-                        const uint32_t w4 = w >> 4;
-                        uint32_t o[4];
+                    for (int r = 0; r < 2; ++r) {
+                        const int qt = kBlocks * tq + r2 + r;        // 32-row block: word rows 4*qt .. 4*qt+3
+                        const uint32_t* wp = wt + (qt >> 1) * 8 * BN;   // its 64-row half's 8 word rows
+                        const int half = qt & 1;
+                        const int srow = g <= BK ? (qt * 32) / g : 0;   // the block's scale row in the stage
+                        if constexpr (kMx) {
+                            uint32_t v[16];
+                            mx::operand_column_regs<BN>(wp, d, half, reinterpret_cast<const uint8_t*>(st)[srow * BN + d], v);
 #pragma unroll
-                        for (int b = 0; b < 4; ++b) {
-                            // byte b of w -> low half, byte b of (w >> 4) -> high half:
-                            // halves (magic + q[8c + 2b], magic + q[8c + 2b + 1])
-                            const uint32_t h = and_or(prmt(w, w4, static_cast<uint32_t>(b | ((4 + b) << 8))),
-                                                      0x000F000Fu, Dq<kBf16>::kMagic);
-                            o[b] = Dq<kBf16>::mul2(Dq<kBf16>::sub2(h, zz), ss);
+                            for (int u = 0; u < 16; ++u) o[16 * r + u] = v[u];
+                            continue;
                         }
-                        const uint32_t dst = b_row + (static_cast<uint32_t>(c ^ (d & 7)) << 4);
-                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(o[0]), "r"(o[1]),
-                                     "r"(o[2]), "r"(o[3])
-                                     : "memory");
+                        const uint32_t s16 = st[srow * BN + d];
+                        const uint32_t z4 = kSym ? 8u : ((zt[srow * (BN / 8) + (d >> 3)] >> (4 * (d & 7))) & 0xFu);
+                        const uint32_t ss = s16 | (s16 << 16);
+                        const uint32_t zz = Dq<kBf16>::kMagic | z4 | (z4 << 16);
+#pragma unroll
+                        for (int cc = 0; cc < 4; ++cc) {
+                            const uint32_t w = wp[(half * 4 + cc) * BN + d];
+                            const uint32_t w4 = w >> 4;
+#pragma unroll
+                            for (int b = 0; b < 4; ++b) {
+                                // byte b of w -> low half, byte b of (w >> 4) -> high half:
+                                // halves (magic + q[8c + 2b], magic + q[8c + 2b + 1])
+                                const uint32_t h = and_or(prmt(w, w4, static_cast<uint32_t>(b | ((4 + b) << 8))),
+                                                          0x000F000Fu, Dq<kBf16>::kMagic);
+                                o[16 * r + 4 * cc + b] = Dq<kBf16>::mul2(Dq<kBf16>::sub2(h, zz), ss);
+                            }
+                        }
                     }
+                    tmem_st_32x32b_x32(op + static_cast<uint32_t>(kBlocks * tq + r2) * 16u, o);
                 }
-                // the MMA (async proxy) reads these writes
-                fence_proxy_async_smem();
+                tmem_wait_st();
+                // the MMA (another thread) reads these tensor-memory writes
+                tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&bars->bfull[bs]));
+                if (lane == 0) mbar_arrive(smem_u32(&bars->afull[as]));
                 advance();
             }
         }
@@ -543,13 +576,13 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_cons
     __syncthreads();
     if (warp == 2) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, C::kTmemCols);
+        tmem_dealloc(tmem_base, kTmemCols);
     }
 }
 
 template <bool kBf16, bool kSym, int MP, bool kMx = false>
 cudaError_t launch_mp(const void* x, const uint32_t* qw, const void* sc, const uint32_t* qz, void* y, int M, int N,
-                      int K, int g, void* workspace, const DeviceProps& dp, cudaStream_t s) {
+                      int K, int g, float* partials, uint32_t* tickets, const DeviceProps& dp, cudaStream_t s) {
     auto kern = gemm_skinny_kernel<kBf16, kSym, MP, kMx>;
     constexpr size_t kSmem = smem_bytes<MP>();
     static_assert(kSmem <= 227 * 1024, "shared memory budget");
@@ -563,23 +596,37 @@ cudaError_t launch_mp(const void* x, const uint32_t* qw, const void* sc, const u
     if (!encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_INT32, qw, (uint64_t)N, (uint64_t)(K / 8), (uint64_t)N * 4, BN,
                    BK / 8, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
+    // scales [K/g, N] (MXFP4: exponent bytes [K/32, N]) and packed zero-points [K/g, N/8]: boxes of
+    // the rows one K step uses by 128 columns
+    CUtensorMap ts, tz;
+    const uint32_t srows = g <= BK ? BK / g : 1;
+    const CUtensorMapDataType sdt = kMx ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : adt;
+    if (!encode_2d(&ts, sdt, sc, (uint64_t)N, (uint64_t)(K / g), (uint64_t)N * (kMx ? 1 : 2), BN, srows,
+                   CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    const bool z_tma = !kSym && N % 32 == 0;   // zero-point rows a multiple of 16 bytes
+    if (z_tma) {
+        if (!encode_2d(&tz, CU_TENSOR_MAP_DATA_TYPE_INT32, qz, (uint64_t)(N / 8), (uint64_t)(K / g),
+                       (uint64_t)(N / 8) * 4, BN / 8, srows, CU_TENSOR_MAP_SWIZZLE_NONE))
+            return cudaErrorInvalidValue;
+    } else {
+        memset(&tz, 0, sizeof(tz));
+    }
     const int tiles = (N + BN - 1) / BN;
     const long long units = static_cast<long long>(tiles) * ((K + BK - 1) / BK);
     const bool streamk = M <= kStreamKMaxM;
     const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(streamk ? units : tiles, dp.sms)));
-    float* partials = static_cast<float*>(workspace);
-    uint32_t* tickets = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(workspace) + skinny_partial_bytes(dp));
-    kern<<<grid, kThreads, kSmem, s>>>(tx, tw, static_cast<const uint16_t*>(sc), qz, static_cast<uint16_t*>(y), M, N, K,
-                                       g, partials, tickets, streamk ? 1 : 0);
+    kern<<<grid, kThreads, kSmem, s>>>(tx, tw, ts, tz, qz, static_cast<uint16_t*>(y), M, N, K, g, partials, tickets,
+                                       streamk ? 1 : 0, z_tma ? 1 : 0);
     return cudaGetLastError();
 }
 
 template <bool kBf16, bool kSym, bool kMx = false>
 cudaError_t launch_typed(const void* x, const uint32_t* qw, const void* sc, const uint32_t* qz, void* y, int M, int N,
-                         int K, int g, void* ws, const DeviceProps& dp, cudaStream_t s) {
-    if (M <= 32) return launch_mp<kBf16, kSym, 32, kMx>(x, qw, sc, qz, y, M, N, K, g, ws, dp, s);
-    if (M <= 64) return launch_mp<kBf16, kSym, 64, kMx>(x, qw, sc, qz, y, M, N, K, g, ws, dp, s);
-    return launch_mp<kBf16, kSym, 128, kMx>(x, qw, sc, qz, y, M, N, K, g, ws, dp, s);
+                         int K, int g, float* pt, uint32_t* tk, const DeviceProps& dp, cudaStream_t s) {
+    if (M <= 32) return launch_mp<kBf16, kSym, 32, kMx>(x, qw, sc, qz, y, M, N, K, g, pt, tk, dp, s);
+    if (M <= 64) return launch_mp<kBf16, kSym, 64, kMx>(x, qw, sc, qz, y, M, N, K, g, pt, tk, dp, s);
+    return launch_mp<kBf16, kSym, 128, kMx>(x, qw, sc, qz, y, M, N, K, g, pt, tk, dp, s);
 }
 
 }  // namespace
@@ -588,26 +635,28 @@ size_t skinny_partial_bytes(const DeviceProps& dp) {
     return static_cast<size_t>(dp.sms) * 2 * kSlotFloats * sizeof(float);
 }
 
-size_t skinny_workspace_bytes(int N, const DeviceProps& dp) {
+size_t skinny_ticket_bytes(int N) {
     // one ticket per column block and epilogue warp
-    const size_t tickets = (static_cast<size_t>((N + BN - 1) / BN) * 4 * sizeof(uint32_t) + 255) & ~size_t(255);
-    return skinny_partial_bytes(dp) + tickets;
+    return (static_cast<size_t>((N + BN - 1) / BN) * 4 * sizeof(uint32_t) + 255) & ~size_t(255);
 }
 
+size_t skinny_workspace_bytes(int N, const DeviceProps& dp) { return skinny_partial_bytes(dp) + skinny_ticket_bytes(N); }
+
 cudaError_t launch_gemm_skinny(const void* x, const uint32_t* qw, const void* sc, const uint32_t* qz, void* y, int M,
-                               int N, int K, int g, bool bf16, void* ws, const DeviceProps& dp, cudaStream_t s) {
-    if (M < 1 || M > kSkinnyMaxM || M > 128 || !ws) return cudaErrorInvalidValue;
+                               int N, int K, int g, bool bf16, float* pt, uint32_t* tk, const DeviceProps& dp,
+                               cudaStream_t s) {
+    if (M < 1 || M > kSkinnyMaxM || M > 128 || !pt || !tk) return cudaErrorInvalidValue;
     if (bf16)
-        return qz ? launch_typed<true, false>(x, qw, sc, qz, y, M, N, K, g, ws, dp, s)
-                  : launch_typed<true, true>(x, qw, sc, qz, y, M, N, K, g, ws, dp, s);
-    return qz ? launch_typed<false, false>(x, qw, sc, qz, y, M, N, K, g, ws, dp, s)
-              : launch_typed<false, true>(x, qw, sc, qz, y, M, N, K, g, ws, dp, s);
+        return qz ? launch_typed<true, false>(x, qw, sc, qz, y, M, N, K, g, pt, tk, dp, s)
+                  : launch_typed<true, true>(x, qw, sc, qz, y, M, N, K, g, pt, tk, dp, s);
+    return qz ? launch_typed<false, false>(x, qw, sc, qz, y, M, N, K, g, pt, tk, dp, s)
+              : launch_typed<false, true>(x, qw, sc, qz, y, M, N, K, g, pt, tk, dp, s);
 }
 
 cudaError_t launch_mx_gemm_skinny(const void* x, const uint32_t* qw, const uint8_t* es, void* y, int M, int N, int K,
-                                  void* ws, const DeviceProps& dp, cudaStream_t s) {
-    if (M < 1 || M > kSkinnyMaxM || M > 128 || !ws) return cudaErrorInvalidValue;
-    return launch_typed<true, true, true>(x, qw, es, nullptr, y, M, N, K, mx::kBlock, ws, dp, s);
+                                  float* pt, uint32_t* tk, const DeviceProps& dp, cudaStream_t s) {
+    if (M < 1 || M > kSkinnyMaxM || M > 128 || !pt || !tk) return cudaErrorInvalidValue;
+    return launch_typed<true, true, true>(x, qw, es, nullptr, y, M, N, K, mx::kBlock, pt, tk, dp, s);
 }
 
 }  // namespace w4a16

@@ -779,7 +779,8 @@ size_t gemv_workspace_bytes(const GemvPlan& p) { return p.ticket_bytes + p.parti
 GemvPlan plan_mx_gemv(int M, int N, int K, const DeviceProps& dp) { return plan(M, N, K, false, dp); }
 
 cudaError_t launch_gemv(const void* x, const uint32_t* qw, const void* sc, const uint32_t* qz, void* y, int M,
-                        int N, int K, int g, bool bf16, const GemvPlan& plan, void* workspace, cudaStream_t s) {
+                        int N, int K, int g, bool bf16, const GemvPlan& plan, float* partials, uint32_t* tickets,
+                        cudaStream_t s) {
     GemvArgs a;
     const CUtensorMapDataType act = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     const uint32_t cb = static_cast<uint32_t>(plan.cb);
@@ -800,8 +801,8 @@ cudaError_t launch_gemv(const void* x, const uint32_t* qw, const void* sc, const
     a.x = static_cast<const uint16_t*>(x);
     a.qz = qz;
     a.y = static_cast<uint16_t*>(y);
-    a.partials = static_cast<float*>(workspace);
-    a.tickets = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(workspace) + plan.partial_bytes);
+    a.partials = partials;
+    a.tickets = tickets;
     a.M = M;
     a.N = N;
     a.K = K;
@@ -812,7 +813,7 @@ cudaError_t launch_gemv(const void* x, const uint32_t* qw, const void* sc, const
 }
 
 cudaError_t launch_mx_gemv(const void* x, const uint32_t* qw, const uint8_t* es, void* y, int M, int N, int K,
-                           const GemvPlan& plan, void* workspace, cudaStream_t s) {
+                           const GemvPlan& plan, float* partials, uint32_t* tickets, cudaStream_t s) {
     if (plan.fact) return cudaErrorInvalidValue;   // the plan must come from plan_mx_gemv
     GemvArgs a;
     const uint32_t cb = static_cast<uint32_t>(plan.cb);
@@ -827,8 +828,8 @@ cudaError_t launch_mx_gemv(const void* x, const uint32_t* qw, const uint8_t* es,
     a.x = static_cast<const uint16_t*>(x);
     a.qz = nullptr;
     a.y = static_cast<uint16_t*>(y);
-    a.partials = static_cast<float*>(workspace);
-    a.tickets = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(workspace) + plan.partial_bytes);
+    a.partials = partials;
+    a.tickets = tickets;
     a.M = M;
     a.N = N;
     a.K = K;

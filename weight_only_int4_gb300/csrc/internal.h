@@ -51,14 +51,27 @@ GemvPlan plan_gemv(int M, int N, int K, int g, const DeviceProps& dp);
 // The GEMV plan for MXFP4 weights (no zero-points); same workspace size as
 // plan_gemv(M, N, K, 32, dp).
 GemvPlan plan_mx_gemv(int M, int N, int K, const DeviceProps& dp);
+// The CUDA-core kernel's own scratch: plan.partial_bytes of partial-sum slots
+// (a size fixed per device) and plan.ticket_bytes of ticket words.
 size_t gemv_workspace_bytes(const GemvPlan& plan);
 
-// `workspace` holds plan.partial_bytes of partial-sum slots (a size fixed per
-// device) followed by plan.ticket_bytes of ticket words (zero before the first
-// call; every call leaves them zero).
+// `partials`: plan.partial_bytes of partial-sum slots; `tickets`: ticket words
+// (zero before the first call; every call leaves them zero).
 cudaError_t launch_gemv(const void* x, const uint32_t* qw, const void* sc, const uint32_t* qz, void* y,
-                        int M, int N, int K, int g, bool bf16, const GemvPlan& plan, void* workspace,
-                        cudaStream_t s);
+                        int M, int N, int K, int g, bool bf16, const GemvPlan& plan, float* partials,
+                        uint32_t* tickets, cudaStream_t s);
+
+// w4a16_gemv hands M >= kGemvTensorMinM rows to the few-row tensor-core kernel
+// when the layer has at least kGemvTensorMinWeights weights: the CUDA-core
+// GEMV does 8 * M FMAs per packed word and is ALU-bound from M = 5 on.
+// Measured (us per call, GEMV / tensor-core kernel): 43008 x 5376 M=4 61.1 /
+// 68.4, M=5 94.6 / 68.5, M=16 234 / 68.4; 6144 x 2048 M=4 10.2 / 16.4, M=5
+// 17.6 / 16.4; 2048 x 2048 M=16 11.9 / 15.8 (small layers stay on the GEMV).
+constexpr int kGemvTensorMinM = 5;
+constexpr long long kGemvTensorMinWeights = 8ll << 20;
+inline bool gemv_uses_tensor_cores(long long M, long long N, long long K) {
+    return M >= kGemvTensorMinM && N * K >= kGemvTensorMinWeights;
+}
 
 // Size of the GEMV's built-in scratch array (w4a16_gemv_noalloc).
 constexpr size_t kGemvNoAllocScratchBytes = size_t(4) << 20;
@@ -91,9 +104,11 @@ constexpr int kSkinnyMaxM = W4A16_SKINNY_MAX_M;
 // one ticket word per column block and epilogue warp (zero before the first
 // call; every call leaves them zero).
 size_t skinny_partial_bytes(const DeviceProps& dp);
-size_t skinny_workspace_bytes(int N, const DeviceProps& dp);
+size_t skinny_ticket_bytes(int N);
+size_t skinny_workspace_bytes(int N, const DeviceProps& dp);   // partials, then tickets
 cudaError_t launch_gemm_skinny(const void* x, const uint32_t* qw, const void* sc, const uint32_t* qz, void* y, int M,
-                               int N, int K, int g, bool bf16, void* ws, const DeviceProps& dp, cudaStream_t s);
+                               int N, int K, int g, bool bf16, float* partials, uint32_t* tickets,
+                               const DeviceProps& dp, cudaStream_t s);
 cudaError_t read_and_clear_skinny_error(uint32_t* out);
 cudaError_t launch_dequant(const uint32_t* qw, const void* sc, const uint32_t* qz, void* out, int N, int K, int g,
                            bool bf16, const DeviceProps& dp, cudaStream_t s);
@@ -104,8 +119,30 @@ cudaError_t launch_mx_dequant(const uint32_t* qw, const uint8_t* es, void* out, 
 cudaError_t launch_mx_gemm(const void* x, const uint32_t* qw, const uint8_t* es, void* y, int M, int N, int K,
                            const DeviceProps& dp, cudaStream_t s);
 cudaError_t launch_mx_gemm_skinny(const void* x, const uint32_t* qw, const uint8_t* es, void* y, int M, int N, int K,
-                                  void* ws, const DeviceProps& dp, cudaStream_t s);
+                                  float* partials, uint32_t* tickets, const DeviceProps& dp, cudaStream_t s);
 cudaError_t launch_mx_gemv(const void* x, const uint32_t* qw, const uint8_t* es, void* y, int M, int N, int K,
-                           const GemvPlan& plan, void* workspace, cudaStream_t s);
+                           const GemvPlan& plan, float* partials, uint32_t* tickets, cudaStream_t s);
+
+// Workspace of the GEMV entry points, which run either the CUDA-core kernel or
+// (5..16 rows of a large layer) the few-row tensor-core kernel: both kernels'
+// partial-sum regions (sizes fixed per device), then one ticket region both
+// use. Every call leaves the tickets at zero and no partial region covers
+// them, so one workspace sized for the largest N serves calls of any shape.
+struct GemvWorkspace {
+    size_t cuda_partials = 0, tensor_partials = 0, tickets = 0;
+    size_t total() const { return cuda_partials + tensor_partials + tickets; }
+    float* cuda_part(void* ws) const { return static_cast<float*>(ws); }
+    float* tensor_part(void* ws) const { return reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + cuda_partials); }
+    uint32_t* ticket_words(void* ws) const {
+        return reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + cuda_partials + tensor_partials);
+    }
+};
+inline GemvWorkspace gemv_workspace(const GemvPlan& plan, int N, const DeviceProps& dp) {
+    GemvWorkspace w;
+    w.cuda_partials = plan.partial_bytes;
+    w.tensor_partials = skinny_partial_bytes(dp);
+    w.tickets = plan.ticket_bytes > skinny_ticket_bytes(N) ? plan.ticket_bytes : skinny_ticket_bytes(N);
+    return w;
+}
 
 }  // namespace w4a16

@@ -143,5 +143,34 @@ __device__ __forceinline__ void operand_column(const uint32_t* wt, uint32_t b_ro
         emit(std::false_type{});
 }
 
+// The same 32 codes as 16 bf16 pairs in registers (pair 4cc + b holds codes
+// 8cc + 2b and 8cc + 2b + 1 of the half), for an operand kept in tensor memory.
+template <int kCols>
+__device__ __forceinline__ void operand_column_regs(const uint32_t* wt, int d, int half, uint32_t e,
+                                                    uint32_t (&o)[16]) {
+    auto emit = [&](auto fast_path) {
+        constexpr bool kFast = decltype(fast_path)::value;
+        const uint32_t fa = kFast ? fast_scale(e) * 0x10001u : kTwoPow126x2;
+        const uint32_t fb = exact_scale(e) * 0x10001u;
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+            const uint32_t w = wt[(half * 4 + cc) * kCols + d];
+            const uint32_t w4 = w >> 4;
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                uint32_t h;
+                asm("prmt.b32 %0, %1, %2, %3;" : "=r"(h) : "r"(w), "r"(w4), "r"(static_cast<uint32_t>(b | ((4 + b) << 8))));
+                uint32_t v = mul_bf16x2(e2m1x2_scaled(h & 0x000F000Fu), fa);
+                if constexpr (!kFast) v = mul_bf16x2(v, fb);
+                o[4 * cc + b] = v;
+            }
+        }
+    };
+    if (fast(e))
+        emit(std::true_type{});
+    else
+        emit(std::false_type{});
+}
+
 }  // namespace mx
 }  // namespace w4a16
