@@ -115,7 +115,7 @@ w4a16_status w4a16_unpack(const int32_t* src, uint8_t* dst, int64_t rows, int64_
 /*
  * w4a16_workspace_bytes -- bytes of device workspace `op` needs for this shape
  * on the current device. For the GEMV: the FP32 partial-sum slots of its
- * CUDA-core kernel (8 KB per SM), then those of the few-row tensor-core kernel
+ * CUDA-core kernel (4 KB per SM), then those of the few-row tensor-core kernel
  * it runs for 5..16 rows of large layers (128 KB per SM; both sizes depend
  * only on the device), then the ticket words of whichever kernel needs more
  * for this shape (one per column block, or four per 128 columns; rounded up
@@ -143,9 +143,9 @@ size_t w4a16_workspace_bytes(w4a16_op op, int64_t M, int64_t N, int64_t K, int64
  * loads of the next 32-row chunk of K are in flight while the current one is
  * converted, which is the overlap whose absence the zero-point page blames for
  * its batch-4, g=128 regression (section "Known regression"). A persistent
- * grid (as many CTAs per SM as shared memory allows, at most two) takes equal
- * shares of (column block, K chunk) items, so every SM streams the same
- * bytes; a column block shared by several CTAs is finished by the last of
+ * grid (one CTA per SM at most) takes equal shares of (column block, K chunk)
+ * items, so every SM streams the same bytes (for small layers, a whole number
+ * of CTAs per column block when that is cheaper); a column block shared by several CTAs is finished by the last of
  * them to arrive, which sums the partial vectors in ascending CTA order: the
  * result is deterministic.
  *
@@ -207,9 +207,9 @@ w4a16_status w4a16_gemv(const void* x, const int32_t* qweight, const void* scale
  *   and give wrong results: serialise them.
  * - A shape whose scratch (w4a16_workspace_bytes(W4A16_OP_GEMV, ...)) exceeds
  *   4 MiB is rejected with W4A16_ERR_WORKSPACE; the partial-sum region takes
- *   8 KB per SM and each column block a 4-byte ticket (column blocks are 32
+ *   4 KB per SM and each column block a 4-byte ticket (column blocks are 32
  *   columns wide for 9 <= M <= 16 and wider for smaller M), so on a 152-SM
- *   GB300 every N up to about 23 million columns fits.
+ *   GB300 every N up to about 28 million columns fits.
  * It always runs the CUDA-core GEMV kernel (the tensor-core kernel's scratch
  * does not fit the array), so its results are identical to w4a16_gemv's
  * wherever w4a16_gemv runs that kernel too: M <= 4, or fewer than 8 Mi

@@ -9,9 +9,11 @@
 // converted. Here:
 //
 //   * Work items are (column block, 32-row chunk of K) pairs, ordered column
-//     block first. A persistent grid of exactly two CTAs per SM takes equal
+//     block first. A persistent grid of at most one CTA per SM takes equal
 //     contiguous ranges of items ("stream-K"), so every SM streams the same
-//     number of bytes whatever N and K are.
+//     number of bytes whatever N and K are. When CTAs have few chunks per
+//     warp, a grid of a whole number of CTAs per column block is taken
+//     instead if it is cheaper: no range then crosses a block boundary.
 //   * Inside a CTA the warps take the chunks of the current column block in
 //     turn. Each warp streams its chunks through its own kStages-deep ring in
 //     shared memory: one lane issues bulk asynchronous copies (TMA, completion
@@ -719,9 +721,13 @@ cudaError_t launch_mx_rows(const GemvArgs& a, const GemvPlan& p, cudaStream_t s)
 }  // namespace
 
 constexpr int kMaxLive = 512;         // max over row templates of M * columns per block
+// Chunks per warp that crossing a column block boundary costs a CTA (fitted to
+// timings: 2 x 16384 x 5376 says more than 1.7, 3 x 5376 x 21504 less than 2.4).
+constexpr double kStraddleCost = 2.0;
 
+// two partial slots (head and tail segment) per CTA, at most one CTA per SM
 size_t partial_region_bytes(const DeviceProps& dp) {
-    return static_cast<size_t>(2) * dp.sms * 2 * kMaxLive * sizeof(float);
+    return static_cast<size_t>(dp.sms) * 2 * kMaxLive * sizeof(float);
 }
 
 namespace {
@@ -743,10 +749,24 @@ GemvPlan plan(int M, int N, int K, bool fact, const DeviceProps& dp) {
     auto size_grid = [&](int xsum_entries) {
         p.smem_bytes = ring_offset(live, xsum_entries) + 128 +
                        static_cast<size_t>(kWarps) * kStages * stage_bytes(p.cols, p.mt);
-        // as many CTAs per SM as shared memory allows (at most 2), each with at least one chunk per warp
-        const int per_sm = p.smem_bytes * 2 <= dp.smem_optin ? 2 : 1;
-        const long long want = static_cast<long long>(per_sm) * dp.sms;
+        // One CTA per SM: every row template needs more than 64 registers a
+        // thread, so two 512-thread CTAs never fit on one SM together, and a
+        // larger grid runs as a second, partial wave. At least one chunk per warp.
+        const long long want = dp.sms;
         p.grid = static_cast<int>(std::max<long long>(1, std::min<long long>(want, items / kWarps)));
+        // A CTA whose range crosses a column block boundary runs the two
+        // segments one after the other (second pipeline fill, second reduction
+        // and fix-up): about kStraddleCost chunks per warp, measured. A grid of
+        // `sp` CTAs per column block never crosses one; take it when its chunks
+        // per warp are fewer than the stream-K grid's plus that cost.
+        const long long sp = std::min<long long>(want / p.n_cb, chunks / kWarps);
+        if (sp >= 1 && p.n_cb * sp != p.grid) {
+            const long long aligned = p.n_cb * sp;
+            // compare items / (grid * kWarps) + kStraddleCost with items / (aligned * kWarps)
+            const double cost_sk = static_cast<double>(items) / (static_cast<double>(p.grid) * kWarps) + kStraddleCost;
+            const double cost_al = static_cast<double>(items) / (static_cast<double>(aligned) * kWarps);
+            if (cost_al < cost_sk) p.grid = static_cast<int>(aligned);
+        }
     };
     size_grid(0);
     // Precomputed chunk sums: a prologue over all chunks, against a warp

@@ -34,7 +34,7 @@ struct GemvPlan {
     int cb = 0;             // columns per column block (32 * cols)
     int n_cb = 0;           // column blocks
     int warps = 0;          // warps per CTA (streaming warps + one reduction warp)
-    int grid = 0;           // persistent CTAs (two per SM at most)
+    int grid = 0;           // persistent CTAs (one per SM at most)
     long long items = 0;    // column blocks x 32-row chunks of K
     long long items_split = 0;   // items of the blocks shared stream-K by all CTAs ([0, whole_first))
     int whole_first = 0;    // first of the blocks handed out whole
