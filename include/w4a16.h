@@ -130,12 +130,14 @@ size_t w4a16_workspace_bytes(w4a16_op op, int64_t M, int64_t N, int64_t K, int64
 /*
  * w4a16_gemv -- decode path, 1 <= M <= 16.
  *
- * With M >= 5 rows and at least 8 Mi weights (N * K >= 8 * 2^20) the call
- * runs the few-row tensor-core kernel of w4a16_gemm instead of the CUDA-core
- * kernel described below: the CUDA-core kernel spends 8 * M FMAs on every
- * packed word and is ALU-bound from M = 5 on (measured at N = 43008,
- * K = 5376: 94.6 against 68.5 us at M = 5, 234 against 68.4 us at M = 16).
- * Smaller layers stay on CUDA cores for every M. Both kernels keep their
+ * With M >= 5 rows of a large enough layer the call runs the few-row
+ * tensor-core kernel of w4a16_gemm instead of the CUDA-core kernel described
+ * below: N * K >= 64 * 2^20 weights for M = 5..6, 36 * 2^20 for M = 7..8,
+ * 24 * 2^20 for M = 9..12 and 10 * 2^20 for M = 13..16. The CUDA-core kernel
+ * spends 8 * M FMAs on every packed word and is ALU-bound from M = 5 on; the
+ * tensor-core kernel's time is flat in M with a floor of about 15 us
+ * (measured at N = 43008, K = 5376: 87.6 against 67.4 us at M = 5; at
+ * N = 4096, K = 2048, M = 16: 11.4 against 15.8 us). Both kernels keep their
  * partial sums in separate regions of the workspace and share its ticket
  * words, which every call leaves at zero.
  *
@@ -212,9 +214,9 @@ w4a16_status w4a16_gemv(const void* x, const int32_t* qweight, const void* scale
  *   GB300 every N up to about 28 million columns fits.
  * It always runs the CUDA-core GEMV kernel (the tensor-core kernel's scratch
  * does not fit the array), so its results are identical to w4a16_gemv's
- * wherever w4a16_gemv runs that kernel too: M <= 4, or fewer than 8 Mi
- * weights; for 5..16 rows of a larger layer they agree within the parity
- * tolerance but are slower. Other errors as
+ * wherever w4a16_gemv runs that kernel too: M <= 4, or a layer below the
+ * thresholds given there; for 5..16 rows of a larger layer they agree within
+ * the parity tolerance but are slower. Other errors as
  * for w4a16_gemv.
  */
 w4a16_status w4a16_gemv_noalloc(const void* x, const int32_t* qweight, const void* scales,
@@ -313,8 +315,8 @@ w4a16_status w4a16_mxfp4_dequant(const int32_t* qweight, const uint8_t* escale, 
  * w4a16_gemv kernel with the E2M1 decode in place of the 4-bit integer one
  * (each 32-row chunk is one exponent block; its scale 2^(e - 127) is applied
  * in FP32 once per chunk). Same persistent grid, deterministic fix-up and
- * programmatic launch; like w4a16_gemv, 5..16 rows of a layer with at least
- * 8 Mi weights run the few-row tensor-core kernel of w4a16_mxfp4_gemm instead.
+ * programmatic launch; like w4a16_gemv (same thresholds), 5..16 rows of a
+ * large enough layer run the few-row tensor-core kernel of w4a16_mxfp4_gemm.
  * Workspace: at least w4a16_workspace_bytes(W4A16_OP_GEMV, M, N, K, 32) bytes,
  * with the same ownership and zero-fill rules as for w4a16_gemv.
  */

@@ -229,12 +229,19 @@ def test_gemv_workspace_reuse_across_shapes():
             assert_within_tol(y, dc.reference(), "f16", "reuse")
 
 
+# (M, smallest layer w4a16_gemv hands to the tensor-core kernel at that M)
+TENSOR_MIN_WEIGHTS = {5: 64 << 20, 6: 64 << 20, 7: 36 << 20, 8: 36 << 20, 12: 24 << 20, 16: 10 << 20}
+
+
 def test_gemv_workspace_shared_by_both_kernels():
     """Calls that run the CUDA-core GEMV and calls that run the few-row
     tensor-core kernel, alternating on one workspace: partial sums of either
     never land on the ticket words the other relies on."""
     cases = [DeviceCase(make_case(M, N, K, 32, "bf16", False, seed=M + N))
-             for (M, N, K) in ((16, 8192, 1024), (1, 4104, 2048), (8, 43008, 256), (3, 1032, 4096))]
+             for (M, N, K) in ((16, 10248, 1024), (1, 4104, 2048), (8, 43008, 896), (3, 1032, 4096))]
+    # the first and third run the tensor-core kernel, the others the CUDA-core one
+    assert [dc.case.N * dc.case.K >= TENSOR_MIN_WEIGHTS.get(dc.case.M, 1 << 62) for dc in cases] == \
+        [True, False, True, False]
     need = max(w4.workspace_bytes(w4.OP_GEMV, dc.case.M, dc.case.N, dc.case.K, 32) for dc in cases)
     ws = w4.new_workspace(need)
     for _ in range(3):
@@ -273,13 +280,14 @@ def test_binding_rejections():
     assert e.value.status == w4.ERR_SHAPE
 
 
-@pytest.mark.parametrize("M,N,K,g,act", [(5, 4104, 2048, 32, "f16"), (8, 8192, 1024, 128, "bf16"),
-                                         (16, 2056, 4096, 64, "f16"), (12, 43008, 256, 32, "bf16")])
+@pytest.mark.parametrize("M,N,K,g,act", [(5, 16392, 4096, 32, "f16"), (8, 9216, 4096, 128, "bf16"),
+                                         (16, 2056, 5120, 64, "f16"), (12, 43008, 640, 32, "bf16")])
 def test_gemv_tensor_core_rows(M, N, K, g, act):
-    """w4a16_gemv hands 5..16 rows of a layer with at least 8 Mi weights to the
-    few-row tensor-core kernel (workspace sized by w4a16_workspace_bytes for
-    the GEMV): parity with the oracle, and two calls bit-identical."""
-    assert N * K >= 8 << 20
+    """w4a16_gemv hands 5..16 rows of a large enough layer (64 Mi weights at
+    5-6 rows down to 10 Mi at 13-16) to the few-row tensor-core kernel
+    (workspace sized by w4a16_workspace_bytes for the GEMV): parity with the
+    oracle, and two calls bit-identical."""
+    assert N * K >= TENSOR_MIN_WEIGHTS[M]
     dc = DeviceCase(make_case(M, N, K, g, act, False, seed=M * 3 + g))
     need = w4.workspace_bytes(w4.OP_GEMV, M, N, K, g)
     assert need > w4.workspace_bytes(w4.OP_GEMM, M, N, K, g)   # both kernels' partial regions

@@ -129,6 +129,23 @@ def test_mx_gemv_activation_range(M, spread):
     assert_close(y, d.reference(), (M, spread))
 
 
+@pytest.mark.parametrize("M,N,K", [(16, 10256, 1024), (8, 43008, 896)])
+def test_mx_gemv_tensor_core_rows(M, N, K):
+    """Rows of a layer above the hand-over threshold (10 Mi weights at 13..16
+    rows, 36 Mi at 7..8) run the few-row tensor-core kernel: parity with the
+    oracle, guards intact, two calls bit-identical."""
+    case = make_mx_case(M, N, K, seed=M + N)
+    d = MxDevice(case)
+    buf, y, pad = guarded_out(M, N, torch.bfloat16)
+    w4.mxfp4_gemv(d.x, d.qw, d.e, out=y)
+    y2 = w4.mxfp4_gemv(d.x, d.qw, d.e)
+    torch.cuda.synchronize()
+    check_guards(buf, pad)
+    assert torch.equal(y, y2)
+    assert_close(y, d.reference(), (M, N, K))
+    assert w4.device_status() == w4.OK
+
+
 def test_mx_gemv_deterministic():
     case = make_mx_case(1, 4112, 4096, seed=5)
     d = MxDevice(case)

@@ -62,15 +62,21 @@ cudaError_t launch_gemv(const void* x, const uint32_t* qw, const void* sc, const
                         uint32_t* tickets, cudaStream_t s);
 
 // w4a16_gemv hands M >= kGemvTensorMinM rows to the few-row tensor-core kernel
-// when the layer has at least kGemvTensorMinWeights weights: the CUDA-core
-// GEMV does 8 * M FMAs per packed word and is ALU-bound from M = 5 on.
-// Measured (us per call, GEMV / tensor-core kernel): 43008 x 5376 M=4 61.1 /
-// 68.4, M=5 94.6 / 68.5, M=16 234 / 68.4; 6144 x 2048 M=4 10.2 / 16.4, M=5
-// 17.6 / 16.4; 2048 x 2048 M=16 11.9 / 15.8 (small layers stay on the GEMV).
+// when the layer has at least gemv_tensor_min_weights(M) weights: the
+// CUDA-core GEMV does 8 * M FMAs per packed word, so its time grows with the
+// row template (6, 8, 12, 16 rows), while the tensor-core kernel's is flat in
+// M with a floor of about 15 us on small layers. Thresholds from timings of
+// both kernels on 12 layer shapes (2048 x 2048 to 43008 x 5376), e.g. (us,
+// CUDA-core / tensor-core): M=5: 8192 x 8192 28.7 / 28.6, 14336 x 4096 27.0 /
+// 28.4, 16384 x 5376 37.0 / 33.8; M=8: 8192 x 4096 18.7 / 21.3, 11008 x 4096
+// 26.4 / 23.3; M=12: 4096 x 4096 16.0 / 18.2, 8192 x 4096 31.1 / 21.4; M=16:
+// 4096 x 2048 11.4 / 15.8, 6144 x 2048 19.7 / 16.5.
 constexpr int kGemvTensorMinM = 5;
-constexpr long long kGemvTensorMinWeights = 8ll << 20;
+inline long long gemv_tensor_min_weights(long long M) {
+    return M <= 6 ? 64ll << 20 : M <= 8 ? 36ll << 20 : M <= 12 ? 24ll << 20 : 10ll << 20;
+}
 inline bool gemv_uses_tensor_cores(long long M, long long N, long long K) {
-    return M >= kGemvTensorMinM && N * K >= kGemvTensorMinWeights;
+    return M >= kGemvTensorMinM && N * K >= gemv_tensor_min_weights(M);
 }
 
 // Size of the GEMV's built-in scratch array (w4a16_gemv_noalloc).
