@@ -229,19 +229,13 @@ def test_gemv_workspace_reuse_across_shapes():
             assert_within_tol(y, dc.reference(), "f16", "reuse")
 
 
-# (M, smallest layer w4a16_gemv hands to the tensor-core kernel at that M)
-TENSOR_MIN_WEIGHTS = {5: 64 << 20, 6: 64 << 20, 7: 36 << 20, 8: 36 << 20, 12: 24 << 20, 16: 10 << 20}
-
-
-def test_gemv_workspace_shared_by_both_kernels():
-    """Calls that run the CUDA-core GEMV and calls that run the few-row
-    tensor-core kernel, alternating on one workspace: partial sums of either
-    never land on the ticket words the other relies on."""
+def test_gemv_workspace_shared_by_templates():
+    """Calls of different row templates (MMA conversion with 16 rows x 64
+    columns and 8 rows x 128 columns, FMA conversion with 1 row x 256 columns
+    and 6 rows x 64 columns), alternating on one workspace: partial sums of
+    one never land on the ticket words another relies on."""
     cases = [DeviceCase(make_case(M, N, K, 32, "bf16", False, seed=M + N))
-             for (M, N, K) in ((16, 10248, 1024), (1, 4104, 2048), (8, 43008, 896), (3, 1032, 4096))]
-    # the first and third run the tensor-core kernel, the others the CUDA-core one
-    assert [dc.case.N * dc.case.K >= TENSOR_MIN_WEIGHTS.get(dc.case.M, 1 << 62) for dc in cases] == \
-        [True, False, True, False]
+             for (M, N, K) in ((16, 10248, 1024), (1, 4104, 2048), (8, 43008, 896), (6, 1032, 2048))]
     need = max(w4.workspace_bytes(w4.OP_GEMV, dc.case.M, dc.case.N, dc.case.K, 32) for dc in cases)
     ws = w4.new_workspace(need)
     for _ in range(3):
@@ -281,13 +275,13 @@ def test_binding_rejections():
 
 
 @pytest.mark.parametrize("M,N,K,g,act", [(5, 16392, 4096, 32, "f16"), (8, 9216, 4096, 128, "bf16"),
-                                         (16, 2056, 5120, 64, "f16"), (12, 43008, 640, 32, "bf16")])
-def test_gemv_tensor_core_rows(M, N, K, g, act):
-    """w4a16_gemv hands 5..16 rows of a large enough layer (64 Mi weights at
-    5-6 rows down to 10 Mi at 13-16) to the few-row tensor-core kernel
-    (workspace sized by w4a16_workspace_bytes for the GEMV): parity with the
-    oracle, and two calls bit-identical."""
-    assert N * K >= TENSOR_MIN_WEIGHTS[M]
+                                         (16, 2056, 5120, 64, "f16"), (12, 43008, 640, 32, "bf16"),
+                                         (2, 4104, 4096, 64, "bf16"), (7, 776, 8192, 128, "f16")])
+def test_gemv_mma_rows(M, N, K, g, act):
+    """2..16 rows of layers above 4 Mi weights go through the GEMV's
+    tensor-core MMA conversion (8 x-rows x 128 columns up to M = 8, 16 x 64
+    above; ragged column blocks included): parity with the oracle, and two
+    calls bit-identical."""
     dc = DeviceCase(make_case(M, N, K, g, act, False, seed=M * 3 + g))
     need = w4.workspace_bytes(w4.OP_GEMV, M, N, K, g)
     assert need > w4.workspace_bytes(w4.OP_GEMM, M, N, K, g)   # both kernels' partial regions

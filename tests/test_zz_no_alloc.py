@@ -38,6 +38,8 @@ CASES = [
     (3, 264, 256, 32, "f16", True),         # ragged column block, symmetric
     (16, 776, 1024, 64, "bf16", False),
     (1, 4104, 2048, 32, "bf16", False),     # N % 32 != 0: zero-points read per lane
+    (8, 8192, 4096, 128, "f16", False),     # MMA conversion, 8-row template
+    (12, 43008, 640, 32, "bf16", False),    # MMA conversion, 16-row template
 ]
 
 

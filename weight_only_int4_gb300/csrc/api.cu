@@ -180,14 +180,6 @@ w4a16_status w4a16_gemv(const void* x, const int32_t* qweight, const void* scale
     const w4a16::GemvPlan plan = w4a16::plan_gemv((int)M, (int)N, (int)K, (int)g, dp);
     const w4a16::GemvWorkspace wl = w4a16::gemv_workspace(plan, (int)N, dp);
     if (workspace_bytes < wl.total()) return W4A16_ERR_WORKSPACE;
-    if (w4a16::gemv_uses_tensor_cores(M, N, K)) {
-        // 5..16 rows of a large layer: the few-row tensor-core kernel is faster
-        return from_cuda(w4a16::launch_gemm_skinny(x, reinterpret_cast<const uint32_t*>(qweight), scales,
-                                                   reinterpret_cast<const uint32_t*>(qzeros), y, (int)M, (int)N,
-                                                   (int)K, (int)g, dt == W4A16_BF16, wl.tensor_part(workspace),
-                                                   wl.ticket_words(workspace), dp,
-                                                   reinterpret_cast<cudaStream_t>(stream)));
-    }
     return from_cuda(w4a16::launch_gemv(x, reinterpret_cast<const uint32_t*>(qweight), scales,
                                         reinterpret_cast<const uint32_t*>(qzeros), y, (int)M, (int)N, (int)K, (int)g,
                                         dt == W4A16_BF16, plan, wl.cuda_part(workspace), wl.ticket_words(workspace),
@@ -292,7 +284,7 @@ w4a16_status w4a16_mxfp4_gemv(const void* x, const int32_t* qweight, const uint8
     const w4a16::GemvPlan plan = w4a16::plan_mx_gemv((int)M, (int)N, (int)K, dp);
     const w4a16::GemvWorkspace wl = w4a16::gemv_workspace(plan, (int)N, dp);
     if (workspace_bytes < wl.total()) return W4A16_ERR_WORKSPACE;
-    if (w4a16::gemv_uses_tensor_cores(M, N, K))
+    if (w4a16::mx_gemv_uses_tensor_cores(M, N, K))
         return from_cuda(w4a16::launch_mx_gemm_skinny(x, reinterpret_cast<const uint32_t*>(qweight), escale, y, (int)M,
                                                       (int)N, (int)K, wl.tensor_part(workspace),
                                                       wl.ticket_words(workspace), dp,

@@ -72,11 +72,34 @@ namespace {
 #endif
 constexpr int kWarps = W4A16_GEMV_WARPS;
 constexpr int kStages = W4A16_GEMV_STAGES;
+// Ring depth of the MMA templates (8 rows x 128 columns, 16 rows x 64
+// columns): their chunks convert several times faster, so more copies must be
+// in flight to cover the load latency.
+#ifndef W4A16_GEMV_MMA_STAGES8
+#define W4A16_GEMV_MMA_STAGES8 2
+#endif
+#ifndef W4A16_GEMV_MMA_STAGES16
+#define W4A16_GEMV_MMA_STAGES16 2
+#endif
+__host__ __device__ constexpr int ring_stages(bool mma, int mt) {
+    return !mma ? kStages : mt == 8 ? W4A16_GEMV_MMA_STAGES8 : W4A16_GEMV_MMA_STAGES16;
+}
 constexpr int kL2Prefetch = W4A16_GEMV_L2_PREFETCH;
 constexpr int kThreads = kWarps * 32;
 constexpr int kChunk = 32;            // rows of K per chunk
 constexpr int kRowsPerChunk = 4;      // packed word rows per chunk
 constexpr int kFactMaxM = 4;          // zero-point through the chunk's sum of x up to this M
+// W4A16 rows from this M on go through the tensor-core MMA conversion (kMma)
+#ifndef W4A16_GEMV_MMA_MIN_M
+#define W4A16_GEMV_MMA_MIN_M 2
+#endif
+constexpr int kMmaMinM = W4A16_GEMV_MMA_MIN_M;
+// ... except layers of at most kFmaSmallMaxWeights weights with at most
+// kFmaSmallMaxM rows, which stay on FP32 FMAs (measured at 2048 x 2048: M=4
+// 4.98 against 5.13 us, M=8 5.91 against 6.39 us; at 2048 x 2560 and above the
+// MMA conversion wins or ties).
+constexpr int kFmaSmallMaxM = 8;
+constexpr long long kFmaSmallMaxWeights = 4ll << 20;
 constexpr int kXPreMinChunksPerWarp = 8;
 constexpr size_t kXsumSmemLimit = 32 * 1024;
 constexpr unsigned long long kWaitLimitCycles = 4000000000ull;   // ~2 s at 2 GHz
@@ -202,8 +225,8 @@ __host__ __device__ constexpr uint32_t xsum_offset(int live_per_warp) { return k
 __host__ __device__ constexpr uint32_t bar_offset(int live_per_warp, int xsum_entries) {
     return (xsum_offset(live_per_warp) + xsum_entries * 8 + 15) & ~15u;
 }
-__host__ __device__ constexpr uint32_t ring_offset(int live_per_warp, int xsum_entries) {
-    return (bar_offset(live_per_warp, xsum_entries) + kWarps * kStages * 8 + 127) & ~127u;
+__host__ __device__ constexpr uint32_t ring_offset(int live_per_warp, int xsum_entries, int stages) {
+    return (bar_offset(live_per_warp, xsum_entries) + kWarps * stages * 8 + 127) & ~127u;
 }
 
 // First CTA whose item range contains item i (ranges are [b*T/G, (b+1)*T/G)).
@@ -221,9 +244,16 @@ __device__ __forceinline__ long long range_start(int b, long long T, int G) { re
 // kXPre (with kFact): the chunk sums of x are computed for every chunk once per
 // CTA, right after the dependency wait, instead of by a warp reduction in each
 // chunk; worth it when every warp has many chunks to amortise it over.
-template <bool kBf16, int MT, int COLS, bool kSym, bool kFact, bool kZBulk, bool kMx = false, bool kXPre = false>
+// kMma: the products of a chunk go through warp-level m16n8k16 tensor-core
+// MMAs instead of FP32 FMAs (rows 2..16): weights as A (16 columns x 16 k per
+// MMA, (q - z) exact in 16 bits), x as B (8 rows per MMA, rows >= M zero),
+// FP32 accumulators scaled once per chunk.
+template <bool kBf16, int MT, int COLS, bool kSym, bool kFact, bool kZBulk, bool kMx = false, bool kXPre = false,
+          bool kMma = false>
 __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant__ GemvArgs a) {
     static_assert(!kXPre || kFact, "precomputed chunk sums serve the zero-point factorisation");
+    static_assert(!kMma || (!kMx && !kFact && ((MT == 8 && COLS == 4) || (MT == 16 && COLS == 2))),
+                  "MMA conversion: 8 rows x 128 columns or 16 rows x 64 columns, zero-points per nibble pair");
     static_assert(!kMx || (kBf16 && kSym && !kFact && !kZBulk), "MXFP4: bf16, no zero-points");
     static_assert(!kMx || Stage<COLS, MT>::kX - Stage<COLS, MT>::kZ >= 4 * MT, "row factors fit the zero-point block");
     using A = Act<kBf16>;
@@ -244,9 +274,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     float* red = reinterpret_cast<float*>(smem);                                   // [kWarps][E]
     const int xs_entries = kXPre ? M * chunks : 0;
     float2* xsum = reinterpret_cast<float2*>(smem + xsum_offset(E));               // [M][chunks] (kXPre)
-    const uint32_t bars = smem_u32(smem) + bar_offset(E, xs_entries) + warp * kStages * 8;
+    constexpr int kSt = ring_stages(kMma, MT);   // depth of each warp's ring
+    const uint32_t bars = smem_u32(smem) + bar_offset(E, xs_entries) + warp * kSt * 8;
     // rings start on a 128-byte boundary of the shared window (128 bytes of slack are reserved)
-    const uint32_t ring = ((smem_u32(smem) + ring_offset(E, xs_entries) + 127u) & ~127u) + warp * kStages * St::kBytes;
+    const uint32_t ring = ((smem_u32(smem) + ring_offset(E, xs_entries, kSt) + 127u) & ~127u) + warp * kSt * St::kBytes;
 
     // The next kernel of the stream may start its own prologue as this grid's
     // CTAs exit. Before the dependency wait below this grid touches no caller
@@ -254,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     // warp's first chunks.
     griddep_launch_dependents();
     if (lane == 0) {
-        for (int st = 0; st < kStages; ++st) mbar_init(bars + 8 * st, 1);
+        for (int st = 0; st < kSt; ++st) mbar_init(bars + 8 * st, 1);
         fence_mbar_init();
         if (warp == 0) {
             tma_prefetch_desc(&a.tq);
@@ -539,9 +570,85 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
             }
         };
 
+        // kMma: one chunk through tensor-core MMAs. Thread (r, c) = (lane / 4,
+        // lane % 4) takes packed word row c (k = 8c .. 8c + 7) of its columns; a
+        // super tile of 64 columns holds four MMA tiles, tile j mapping MMA row r
+        // to column 4r + j and row r + 8 to column 32 + 4r + j. The nibble pairs
+        // (k, k + 4), (k + 1, k + 5) feed the first MMA's k pairs and (k + 2,
+        // k + 6), (k + 3, k + 7) the second's; x is permuted the same way, so
+        // every product meets its own x. C fragment: column 4r + j (+ 32), rows
+        // m = 8 nt + 2c, 2c + 1.
+        auto compute_mma = [&](int st, int c) {
+          if constexpr (kMma) {
+            constexpr int NT = MT / 8, SU = CB / 64;
+            const uint32_t base = ring + st * St::kBytes;
+            const int r = lane >> 2, tg = lane & 3;
+            uint32_t bx[NT][4];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                uint32_t xw[4];
+                lds<16>(base + St::kX + (8 * nt + r) * kChunk * 2 + tg * 16, xw);   // rows >= M: zero fill
+                bx[nt][0] = __byte_perm(xw[0], xw[2], 0x5410);   // x[k], x[k + 4]
+                bx[nt][1] = __byte_perm(xw[0], xw[2], 0x7632);   // x[k + 1], x[k + 5]
+                bx[nt][2] = __byte_perm(xw[1], xw[3], 0x5410);   // x[k + 2], x[k + 6]
+                bx[nt][3] = __byte_perm(xw[1], xw[3], 0x7632);   // x[k + 3], x[k + 7]
+            }
+#pragma unroll
+            for (int u = 0; u < SU; ++u) {
+                const int c_lo = 64 * u + 4 * r, c_hi = c_lo + 32;   // first of 4 adjacent columns
+                uint32_t q_lo[4], q_hi[4], s_lo[2], s_hi[2];
+                lds<16>(base + St::kQ + (tg * CB + c_lo) * 4, q_lo);
+                lds<16>(base + St::kQ + (tg * CB + c_hi) * 4, q_hi);
+                lds<8>(base + St::kS + c_lo * 2, s_lo);
+                lds<8>(base + St::kS + c_hi * 2, s_hi);
+                uint32_t z_lo = 0u, z_hi = 0u;   // the 4 columns' zero-points: nibbles 0..3
+                if constexpr (!kSym) {
+                    if constexpr (kZBulk) {
+                        uint32_t v[1];
+                        lds<4>(base + St::kZ + (c_lo >> 3) * 4, v);
+                        z_lo = v[0] >> (4 * (c_lo & 7));
+                        lds<4>(base + St::kZ + (c_hi >> 3) * 4, v);
+                        z_hi = v[0] >> (4 * (c_hi & 7));
+                    } else {
+                        const size_t row = static_cast<size_t>((c * kChunk) >> g_shift) * (N >> 3);
+                        const int n_lo = cb * CB + c_lo, n_hi = cb * CB + c_hi;
+                        z_lo = n_lo < N ? __ldg(a.qz + row + (n_lo >> 3)) >> (4 * (n_lo & 7)) : 0u;
+                        z_hi = n_hi < N ? __ldg(a.qz + row + (n_hi >> 3)) >> (4 * (n_hi & 7)) : 0u;
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    // (magic + z) in both halves; the difference with (magic + q) is exact
+                    const uint32_t zl = kSym ? 8u : ((z_lo >> (4 * j)) & 0xFu);
+                    const uint32_t zh = kSym ? 8u : ((z_hi >> (4 * j)) & 0xFu);
+                    const uint32_t zzl = A::kMagic + zl * 0x10001u, zzh = A::kMagic + zh * 0x10001u;
+                    uint32_t hl[4], hh[4];
+#pragma unroll
+                    for (int bb = 0; bb < 4; ++bb) {
+                        hl[bb] = A::sub2(and_or(q_lo[j] >> (4 * bb), 0x000F000Fu, A::kMagic), zzl);
+                        hh[bb] = A::sub2(and_or(q_hi[j] >> (4 * bb), 0x000F000Fu, A::kMagic), zzh);
+                    }
+                    const float sl = A::to_float(static_cast<uint16_t>(s_lo[j >> 1] >> (16 * (j & 1))));
+                    const float sh = A::to_float(static_cast<uint16_t>(s_hi[j >> 1] >> (16 * (j & 1))));
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        float d[4] = {0.f, 0.f, 0.f, 0.f};
+                        mma_m16n8k16<kBf16>(d, hl[0], hh[0], hl[1], hh[1], bx[nt][0], bx[nt][1]);
+                        mma_m16n8k16<kBf16>(d, hl[2], hh[2], hl[3], hh[3], bx[nt][2], bx[nt][3]);
+                        float* y = &yacc[0][0] + ((nt * SU + u) * 4 + j) * 4;
+                        y[0] = fmaf(sl, d[0], y[0]);
+                        y[1] = fmaf(sl, d[1], y[1]);
+                        y[2] = fmaf(sh, d[2], y[2]);
+                        y[3] = fmaf(sh, d[3], y[3]);
+                    }
+                }
+            }
+          }
+        };
+
         // this warp's chunks c0 + warp + kWarps * j, through its kStages-deep ring
         if (elect_one())
-            for (int j = 0; j < kStages && j < nj; ++j) issue(j, c0 + warp + kWarps * j);
+            for (int j = 0; j < kSt && j < nj; ++j) issue(j, c0 + warp + kWarps * j);
         __syncwarp();
         if constexpr (kXPre) {
             if (sums_pending) {   // CTA-uniform: every thread runs the same segments
@@ -551,25 +658,39 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
             }
         }
         for (int j = 0; j < nj; ++j) {
-            const int st = j % kStages;
+            const int st = j % kSt;
             if (!warp_wait(bars + 8 * st, (phase_bits >> st) & 1u, lane)) {
                 ok = false;
                 drain_lo = j;
-                drain_hi = std::min(nj, j + kStages);
+                drain_hi = std::min(nj, j + kSt);
                 break;
             }
             phase_bits ^= 1u << st;
-            compute(st, c0 + warp + kWarps * j);
+            if constexpr (kMma)
+                compute_mma(st, c0 + warp + kWarps * j);
+            else
+                compute(st, c0 + warp + kWarps * j);
             // every lane's reads of the stage precede the copy that refills it
             fence_proxy_async_smem();
             __syncwarp();
-            if (j + kStages < nj && elect_one()) issue(st, c0 + warp + kWarps * (j + kStages));
+            if (j + kSt < nj && elect_one()) issue(st, c0 + warp + kWarps * (j + kSt));
         }
         // partial sums of the warps -> shared memory, reduced in warp order
+        if constexpr (kMma) {
+            constexpr int SU = CB / 64;
+            const int r = lane >> 2, tg = lane & 3;
 #pragma unroll
-        for (int m = 0; m < MT; ++m)
+            for (int i = 0; i < MT * COLS; ++i) {
+                const int e = i & 3, j = (i >> 2) & 3, u = (i >> 4) % SU, nt = (i >> 4) / SU;
+                const int m = 8 * nt + 2 * tg + (e & 1), col = 64 * u + (e >> 1) * 32 + 4 * r + j;
+                red[warp * E + m * CB + col] = (&yacc[0][0])[i];
+            }
+        } else {
 #pragma unroll
-            for (int j = 0; j < COLS; ++j) red[warp * E + m * CB + St::col(lane, j / W, j % W)] = yacc[m][j];
+            for (int m = 0; m < MT; ++m)
+#pragma unroll
+                for (int j = 0; j < COLS; ++j) red[warp * E + m * CB + St::col(lane, j / W, j % W)] = yacc[m][j];
+        }
         __syncthreads();
         const int EM = M * CB;                       // live entries: rows m < M
         for (int e = threadIdx.x; e < EM; e += kThreads) {
@@ -631,7 +752,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     // flight, so none lands in shared memory after the CTA has exited
     if (lane == 0) {
         for (int j = drain_lo; j < drain_hi; ++j) {
-            const int st = j % kStages;
+            const int st = j % kSt;
             const uint32_t par = (phase_bits >> st) & 1u;
             const unsigned long long t0 = clock64();
             while (!mbar_try_wait(bars + 8 * st, par) && clock64() - t0 < kWaitLimitCycles) {
@@ -641,10 +762,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     }
 }
 
-template <bool kBf16, int MT, int COLS, bool kSym, bool kFact, bool kZBulk, bool kMx = false, bool kXPre = false>
+template <bool kBf16, int MT, int COLS, bool kSym, bool kFact, bool kZBulk, bool kMx = false, bool kXPre = false,
+          bool kMma = false>
 cudaError_t launch_one(const GemvArgs& a, const GemvPlan& p, cudaStream_t s) {
     static_assert(Stage<COLS, MT>::kBytes == stage_bytes(COLS, MT), "stage layout");
-    auto kern = gemv_kernel<kBf16, MT, COLS, kSym, kFact, kZBulk, kMx, kXPre>;
+    auto kern = gemv_kernel<kBf16, MT, COLS, kSym, kFact, kZBulk, kMx, kXPre, kMma>;
     const size_t smem = p.smem_bytes;
     if (smem > 48 * 1024) {
         if (cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), p.device, smem); e != cudaSuccess)
@@ -663,16 +785,23 @@ cudaError_t launch_one(const GemvArgs& a, const GemvPlan& p, cudaStream_t s) {
     return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
-template <bool kBf16, int MT, int COLS, bool kFact, bool kXPre = false>
+template <bool kBf16, int MT, int COLS, bool kFact, bool kXPre = false, bool kMma = false>
 cudaError_t launch_sym(const GemvArgs& a, const GemvPlan& p, cudaStream_t s) {
     const bool zb = (a.N % 32) == 0;
-    if (!a.qz) return launch_one<kBf16, MT, COLS, true, kFact, false, false, kXPre>(a, p, s);
-    return zb ? launch_one<kBf16, MT, COLS, false, kFact, true, false, kXPre>(a, p, s)
-              : launch_one<kBf16, MT, COLS, false, kFact, false, false, kXPre>(a, p, s);
+    if (!a.qz) return launch_one<kBf16, MT, COLS, true, kFact, false, false, kXPre, kMma>(a, p, s);
+    return zb ? launch_one<kBf16, MT, COLS, false, kFact, true, false, kXPre, kMma>(a, p, s)
+              : launch_one<kBf16, MT, COLS, false, kFact, false, false, kXPre, kMma>(a, p, s);
 }
 
 template <bool kBf16>
 cudaError_t launch_dtype(const GemvArgs& a, const GemvPlan& p, cudaStream_t s) {
+    if (p.mma) {
+        switch (p.mt) {
+            case 8: return launch_sym<kBf16, 8, 4, false, false, true>(a, p, s);
+            case 16: return launch_sym<kBf16, 16, 2, false, false, true>(a, p, s);
+            default: return cudaErrorInvalidValue;
+        }
+    }
     if (p.fact && p.xpre) {
         switch (p.mt) {
             case 1: return launch_sym<kBf16, 1, 8, true, true>(a, p, s);
@@ -720,10 +849,15 @@ cudaError_t launch_mx_rows(const GemvArgs& a, const GemvPlan& p, cudaStream_t s)
 
 }  // namespace
 
-constexpr int kMaxLive = 512;         // max over row templates of M * columns per block
+constexpr int kMaxLive = 1024;        // max over row templates of M * columns per block
 // Chunks per warp that crossing a column block boundary costs a CTA (fitted to
 // timings: 2 x 16384 x 5376 says more than 1.7, 3 x 5376 x 21504 less than 2.4).
 constexpr double kStraddleCost = 2.0;
+// Fewest chunks a CTA is given (of kWarps = 16 streaming warps). Measured
+// against 16, 4 and 2 (us): 4x2048x2048 6.00 / 5.23 / 5.30 / 5.30 at 16 / 8 /
+// 4 / 2, 1x2048x2048 5.11 / 4.50 / 5.08 / 5.38, 4x1024x4096 6.17 / 5.91 /
+// 6.44 / 6.44.
+constexpr int kMinChunksPerCta = 8;
 
 // two partial slots (head and tail segment) per CTA, at most one CTA per SM
 size_t partial_region_bytes(const DeviceProps& dp) {
@@ -736,30 +870,41 @@ namespace {
 // (the W4A16 layer for M <= 4; never for MXFP4 weights, which have none).
 GemvPlan plan(int M, int N, int K, bool fact, const DeviceProps& dp) {
     GemvPlan p;
-    p.mt = M <= 1 ? 1 : M <= 2 ? 2 : M <= 3 ? 3 : M <= 4 ? 4 : M <= 6 ? 6 : M <= 8 ? 8 : M <= 12 ? 12 : 16;
-    p.cols = p.mt == 1 ? 8 : p.mt <= 4 ? 4 : p.mt <= 8 ? 2 : 1;
+    p.mma = fact && M >= kMmaMinM &&
+            (M > kFmaSmallMaxM || static_cast<long long>(N) * K > kFmaSmallMaxWeights);
+    if (p.mma) {
+        p.mt = M <= 8 ? 8 : 16;
+        p.cols = M <= 8 ? 4 : 2;
+    } else {
+        p.mt = M <= 1 ? 1 : M <= 2 ? 2 : M <= 3 ? 3 : M <= 4 ? 4 : M <= 6 ? 6 : M <= 8 ? 8 : M <= 12 ? 12 : 16;
+        p.cols = p.mt == 1 ? 8 : p.mt <= 4 ? 4 : p.mt <= 8 ? 2 : 1;
+    }
     p.cb = 32 * p.cols;
     p.n_cb = (N + p.cb - 1) / p.cb;
     p.warps = kWarps;
     const int chunks = K / kChunk;
     const long long items = static_cast<long long>(p.n_cb) * chunks;
     p.items = items;
-    p.fact = fact && M <= kFactMaxM;
+    p.fact = fact && M <= kFactMaxM && !p.mma;
     const int live = p.mt * p.cb;
     auto size_grid = [&](int xsum_entries) {
-        p.smem_bytes = ring_offset(live, xsum_entries) + 128 +
-                       static_cast<size_t>(kWarps) * kStages * stage_bytes(p.cols, p.mt);
+        const int stages = ring_stages(p.mma, p.mt);
+        p.smem_bytes = ring_offset(live, xsum_entries, stages) + 128 +
+                       static_cast<size_t>(kWarps) * stages * stage_bytes(p.cols, p.mt);
         // One CTA per SM: every row template needs more than 64 registers a
         // thread, so two 512-thread CTAs never fit on one SM together, and a
-        // larger grid runs as a second, partial wave. At least one chunk per warp.
+        // larger grid runs as a second, partial wave. At least
+        // kMinChunksPerCta chunks per CTA: on a small layer, half the warps of
+        // a CTA busy on twice as many SMs beat every warp busy on half of them
+        // (the conversion of a chunk is issue-bound on the SM's schedulers).
         const long long want = dp.sms;
-        p.grid = static_cast<int>(std::max<long long>(1, std::min<long long>(want, items / kWarps)));
+        p.grid = static_cast<int>(std::max<long long>(1, std::min<long long>(want, items / kMinChunksPerCta)));
         // A CTA whose range crosses a column block boundary runs the two
         // segments one after the other (second pipeline fill, second reduction
         // and fix-up): about kStraddleCost chunks per warp, measured. A grid of
         // `sp` CTAs per column block never crosses one; take it when its chunks
         // per warp are fewer than the stream-K grid's plus that cost.
-        const long long sp = std::min<long long>(want / p.n_cb, chunks / kWarps);
+        const long long sp = std::min<long long>(want / p.n_cb, chunks / kMinChunksPerCta);
         if (sp >= 1 && p.n_cb * sp != p.grid) {
             const long long aligned = p.n_cb * sp;
             // compare items / (grid * kWarps) + kStraddleCost with items / (aligned * kWarps)

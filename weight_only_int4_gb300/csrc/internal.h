@@ -39,6 +39,7 @@ struct GemvPlan {
     long long items_split = 0;   // items of the blocks shared stream-K by all CTAs ([0, whole_first))
     int whole_first = 0;    // first of the blocks handed out whole
     int whole_per_cta = 0;  // whole blocks per CTA (after its stream-K share)
+    bool mma = false;       // products through warp-level tensor-core MMAs (W4A16, 2..16 rows)
     bool fact = false;      // zero-point applied per chunk through chunk sums of x
     bool xpre = false;      // with fact: the chunk sums computed once per CTA up front
     size_t smem_bytes = 0;  // dynamic shared memory per CTA
@@ -61,21 +62,23 @@ cudaError_t launch_gemv(const void* x, const uint32_t* qw, const void* sc, const
                         int M, int N, int K, int g, bool bf16, const GemvPlan& plan, float* partials,
                         uint32_t* tickets, cudaStream_t s);
 
-// w4a16_gemv hands M >= kGemvTensorMinM rows to the few-row tensor-core kernel
-// when the layer has at least gemv_tensor_min_weights(M) weights: the
-// CUDA-core GEMV does 8 * M FMAs per packed word, so its time grows with the
-// row template (6, 8, 12, 16 rows), while the tensor-core kernel's is flat in
-// M with a floor of about 15 us on small layers. Thresholds from timings of
-// both kernels on 12 layer shapes (2048 x 2048 to 43008 x 5376), e.g. (us,
-// CUDA-core / tensor-core): M=5: 8192 x 8192 28.7 / 28.6, 14336 x 4096 27.0 /
+// w4a16_mxfp4_gemv hands M >= kGemvTensorMinM rows to the few-row
+// tensor-core kernel when the layer has at least gemv_tensor_min_weights(M)
+// weights: its GEMV converts with FP32 FMAs (8 * M per packed word), so its
+// time grows with the row template (6, 8, 12, 16 rows), while the tensor-core
+// kernel's is flat in M with a floor of about 15 us on small layers.
+// Thresholds from timings of both kernels on 12 layer shapes (2048 x 2048 to
+// 43008 x 5376) with the same FMA conversion on W4A16 weights, e.g. (us,
+// GEMV / tensor-core): M=5: 8192 x 8192 28.7 / 28.6, 14336 x 4096 27.0 /
 // 28.4, 16384 x 5376 37.0 / 33.8; M=8: 8192 x 4096 18.7 / 21.3, 11008 x 4096
 // 26.4 / 23.3; M=12: 4096 x 4096 16.0 / 18.2, 8192 x 4096 31.1 / 21.4; M=16:
-// 4096 x 2048 11.4 / 15.8, 6144 x 2048 19.7 / 16.5.
+// 4096 x 2048 11.4 / 15.8, 6144 x 2048 19.7 / 16.5. (w4a16_gemv converts 2..16
+// rows with tensor-core MMAs and beats the tensor-core kernel at every M.)
 constexpr int kGemvTensorMinM = 5;
 inline long long gemv_tensor_min_weights(long long M) {
     return M <= 6 ? 64ll << 20 : M <= 8 ? 36ll << 20 : M <= 12 ? 24ll << 20 : 10ll << 20;
 }
-inline bool gemv_uses_tensor_cores(long long M, long long N, long long K) {
+inline bool mx_gemv_uses_tensor_cores(long long M, long long N, long long K) {
     return M >= kGemvTensorMinM && N * K >= gemv_tensor_min_weights(M);
 }
 
@@ -129,10 +132,10 @@ cudaError_t launch_mx_gemm_skinny(const void* x, const uint32_t* qw, const uint8
 cudaError_t launch_mx_gemv(const void* x, const uint32_t* qw, const uint8_t* es, void* y, int M, int N, int K,
                            const GemvPlan& plan, float* partials, uint32_t* tickets, cudaStream_t s);
 
-// Workspace of the GEMV entry points, which run either the CUDA-core kernel or
-// (5..16 rows of a large layer) the few-row tensor-core kernel: both kernels'
-// partial-sum regions (sizes fixed per device), then one ticket region both
-// use. Every call leaves the tickets at zero and no partial region covers
+// Workspace of the GEMV entry points (w4a16_mxfp4_gemv runs either the GEMV
+// kernel or, for 5..16 rows of a large layer, the few-row tensor-core kernel):
+// both kernels' partial-sum regions (sizes fixed per device), then one ticket
+// region both use. Every call leaves the tickets at zero and no partial region covers
 // them, so one workspace sized for the largest N serves calls of any shape.
 struct GemvWorkspace {
     size_t cuda_partials = 0, tensor_partials = 0, tickets = 0;

@@ -352,4 +352,24 @@ __device__ __forceinline__ float fma_mixed(uint32_t w, uint32_t x, float acc) {
     return acc;
 }
 
+// Warp-level D += A * B, m16n8k16, 16-bit A and B of the same type, FP32
+// accumulators (D/C fragment: rows groupID and groupID + 8, columns
+// 2 * threadID_in_group + {0, 1}; A: rows groupID / groupID + 8, k pairs
+// 2 * tig + {0, 1} and + 8; B: k pairs 2 * tig + {0, 1} and + 8, column
+// groupID; the lower k of a pair in the low half of its register).
+template <bool kBf16>
+__device__ __forceinline__ void mma_m16n8k16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                             uint32_t b0, uint32_t b1) {
+    if constexpr (kBf16)
+        asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+            "{%0,%1,%2,%3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    else
+        asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+            "{%0,%1,%2,%3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 }  // namespace w4a16
