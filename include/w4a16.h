@@ -114,12 +114,12 @@ w4a16_status w4a16_unpack(const int32_t* src, uint8_t* dst, int64_t rows, int64_
 
 /*
  * w4a16_workspace_bytes -- bytes of device workspace `op` needs for this shape
- * on the current device. For the GEMV: the FP32 partial-sum slots of its
- * CUDA-core kernel (4 KB per SM), then those of the few-row tensor-core kernel
- * it runs for 5..16 rows of large layers (128 KB per SM; both sizes depend
- * only on the device), then the ticket words of whichever kernel needs more
- * for this shape (one per column block, or four per 128 columns; rounded up
- * to 256 bytes). For the GEMM
+ * on the current device. For the GEMV: the FP32 partial-sum slots of the
+ * GEMV kernel (8 KB per SM), then those of the few-row tensor-core kernel
+ * that w4a16_mxfp4_gemv runs for 5..16 rows of large layers (128 KB per SM;
+ * both sizes depend only on the device), then the ticket words of whichever
+ * kernel needs more for this shape (one per column block, or four per 128
+ * columns; rounded up to 256 bytes). For the GEMM
  * with M <= 128: FP32 partial slots of 128 KB per SM, followed by four 32-bit
  * tickets per 128 columns (rounded up to 256 bytes); 0 for the GEMM with
  * M > 128. The same sizes serve w4a16_mxfp4_gemv and w4a16_mxfp4_gemm with
@@ -130,16 +130,12 @@ size_t w4a16_workspace_bytes(w4a16_op op, int64_t M, int64_t N, int64_t K, int64
 /*
  * w4a16_gemv -- decode path, 1 <= M <= 16.
  *
- * With M >= 5 rows of a large enough layer the call runs the few-row
- * tensor-core kernel of w4a16_gemm instead of the CUDA-core kernel described
- * below: N * K >= 64 * 2^20 weights for M = 5..6, 36 * 2^20 for M = 7..8,
- * 24 * 2^20 for M = 9..12 and 10 * 2^20 for M = 13..16. The CUDA-core kernel
- * spends 8 * M FMAs on every packed word and is ALU-bound from M = 5 on; the
- * tensor-core kernel's time is flat in M with a floor of about 15 us
- * (measured at N = 43008, K = 5376: 87.6 against 67.4 us at M = 5; at
- * N = 4096, K = 2048, M = 16: 11.4 against 15.8 us). Both kernels keep their
- * partial sums in separate regions of the workspace and share its ticket
- * words, which every call leaves at zero.
+ * One row (and up to 8 rows of a layer of at most 4 * 2^20 weights) is
+ * converted with FP32 FMAs; 2..16 rows otherwise go through warp-level
+ * m16n8k16 tensor-core MMAs: (q - z) formed exactly in 16 bits as the A
+ * operand, x as B, FP32 accumulators scaled once per 32-row chunk (measured
+ * at N = 43008, K = 5376: 39.3 us at M = 4 against 58.9 us with FMAs, 59 us
+ * at M = 16 against 67.5 us on the few-row tensor-core kernel of w4a16_gemm).
  *
  * Streams qweight, scales and qzeros once with 128-bit coalesced loads; the
  * loads of the next 32-row chunk of K are in flight while the current one is
@@ -209,15 +205,11 @@ w4a16_status w4a16_gemv(const void* x, const int32_t* qweight, const void* scale
  *   and give wrong results: serialise them.
  * - A shape whose scratch (w4a16_workspace_bytes(W4A16_OP_GEMV, ...)) exceeds
  *   4 MiB is rejected with W4A16_ERR_WORKSPACE; the partial-sum region takes
- *   4 KB per SM and each column block a 4-byte ticket (column blocks are 32
- *   columns wide for 9 <= M <= 16 and wider for smaller M), so on a 152-SM
- *   GB300 every N up to about 28 million columns fits.
- * It always runs the CUDA-core GEMV kernel (the tensor-core kernel's scratch
- * does not fit the array), so its results are identical to w4a16_gemv's
- * wherever w4a16_gemv runs that kernel too: M <= 4, or a layer below the
- * thresholds given there; for 5..16 rows of a larger layer they agree within
- * the parity tolerance but are slower. Other errors as
- * for w4a16_gemv.
+ *   8 KB per SM and each column block a 4-byte ticket (column blocks are at
+ *   least 64 columns wide), so on a 152-SM GB300 every N up to about 47
+ *   million columns fits.
+ * It runs the same kernel and plan as w4a16_gemv, so its results are
+ * identical to w4a16_gemv's. Other errors as for w4a16_gemv.
  */
 w4a16_status w4a16_gemv_noalloc(const void* x, const int32_t* qweight, const void* scales,
                                 const int32_t* qzeros, void* y, int64_t M, int64_t N, int64_t K,
@@ -314,9 +306,12 @@ w4a16_status w4a16_mxfp4_dequant(const int32_t* qweight, const uint8_t* escale, 
  * w4a16_mxfp4_gemv -- decode path for MXFP4 weights, 1 <= M <= 16: the
  * w4a16_gemv kernel with the E2M1 decode in place of the 4-bit integer one
  * (each 32-row chunk is one exponent block; its scale 2^(e - 127) is applied
- * in FP32 once per chunk). Same persistent grid, deterministic fix-up and
- * programmatic launch; like w4a16_gemv (same thresholds), 5..16 rows of a
- * large enough layer run the few-row tensor-core kernel of w4a16_mxfp4_gemm.
+ * in FP32 once per chunk) and FP32 FMAs for every M. Same persistent grid,
+ * deterministic fix-up and programmatic launch. 5..16 rows of a large enough
+ * layer run the few-row tensor-core kernel of w4a16_mxfp4_gemm instead:
+ * N * K >= 64 * 2^20 weights for M = 5..6, 36 * 2^20 for M = 7..8, 24 * 2^20
+ * for M = 9..12 and 10 * 2^20 for M = 13..16 (where the FMA conversion,
+ * 8 * M products per packed word, falls behind).
  * Workspace: at least w4a16_workspace_bytes(W4A16_OP_GEMV, M, N, K, 32) bytes,
  * with the same ownership and zero-fill rules as for w4a16_gemv.
  */
