@@ -45,6 +45,23 @@ def test_gemv_parity(act, g, sym, M):
         parity("gemv", M, N, K, g, act, sym, seed=M + N + K)
 
 
+# Layers just above 4 Mi weights: 2..16 rows run the GEMV's tensor-core MMA
+# conversion (smaller layers keep FP32 FMAs up to 8 rows). One with N % 32 != 0
+# (zero-point words read per lane, ragged last column block), one with N % 32 == 0
+# (zero-point words by tensor copy).
+MMA_LAYERS = [(2056, 2304), (2304, 2048)]
+
+
+@pytest.mark.parametrize("act", ["f16", "bf16"])
+@pytest.mark.parametrize("g", [32, 128, 256])
+@pytest.mark.parametrize("sym", [False, True])
+@pytest.mark.parametrize("M", [2, 3, 4, 5, 8, 9, 13, 16])
+def test_gemv_mma_parity(act, g, sym, M):
+    for (N, K) in MMA_LAYERS:
+        assert N * K > 4 << 20
+        parity("gemv", M, N, K, g, act, sym, seed=3 * M + g + N)
+
+
 @pytest.mark.parametrize("g", [64, 256])
 @pytest.mark.parametrize("M", [1, 5, 11])
 def test_gemv_other_groups(g, M):

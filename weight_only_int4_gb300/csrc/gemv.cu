@@ -46,7 +46,10 @@
 
 #include <algorithm>
 #include <cstring>
+#include <array>
+#include <map>
 #include <mutex>
+#include <tuple>
 
 namespace w4a16 {
 
@@ -211,6 +214,7 @@ struct GemvArgs {
     const uint16_t* x;
     int M, N, K, g_shift;
     int chunks;
+    int cluster;          // > 1: the grid is clusters of this many CTAs, one column block each
     long long items;      // n_cb * chunks
 };
 
@@ -708,6 +712,28 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
         if (c0 == 0 && c1 == chunks) {
             // this CTA owns the whole column block
             for (int e = threadIdx.x; e < EM; e += kThreads) store_y(e, red[e]);
+        } else if (a.cluster > 1) {
+            // The block's CTAs form this cluster, in K order by rank. Once every
+            // CTA's partial is in its red[], rank 0 sums them in rank order (the
+            // ticket path's order, so both give the same bits) through
+            // distributed shared memory; the second barrier keeps the others'
+            // shared memory alive until it has read it.
+            cluster_sync();
+            if (cluster_ctarank() == 0) {
+                const int nc = a.cluster;
+                for (int e = threadIdx.x; e < EM; e += kThreads) {
+                    const uint32_t addr = smem_u32(red + e);
+                    float v[8];
+#pragma unroll
+                    for (int r = 1; r < 8; ++r) v[r] = r < nc ? ld_cluster_f32(addr, r) : 0.f;
+                    float sum = red[e];
+#pragma unroll
+                    for (int r = 1; r < 8; ++r)
+                        if (r < nc) sum += v[r];
+                    store_y(e, sum);
+                }
+            }
+            cluster_sync();
         } else {
             const int slot = c0 > 0 ? 0 : 1;
             float* part = a.partials + (static_cast<size_t>(b) * 2 + slot) * EM;
@@ -762,6 +788,25 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     }
 }
 
+// Whether `clusters` clusters of this launch can all be resident at once
+// (asked once per kernel, cluster size and shared-memory size).
+bool clusters_fit(const void* kern, const cudaLaunchConfig_t& cfg, int clusters) {
+    static std::mutex mu;
+    static std::map<std::tuple<const void*, unsigned, size_t>, int> cache;
+    const auto key = std::make_tuple(kern, cfg.attrs[cfg.numAttrs - 1].val.clusterDim.x, cfg.dynamicSmemBytes);
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(key);
+    if (it == cache.end()) {
+        int active = 0;
+        if (cudaOccupancyMaxActiveClusters(&active, kern, &cfg) != cudaSuccess) {
+            (void)cudaGetLastError();
+            active = 0;
+        }
+        it = cache.emplace(key, active).first;
+    }
+    return it->second >= clusters;
+}
+
 template <bool kBf16, int MT, int COLS, bool kSym, bool kFact, bool kZBulk, bool kMx = false, bool kXPre = false,
           bool kMma = false>
 cudaError_t launch_one(const GemvArgs& a, const GemvPlan& p, cudaStream_t s) {
@@ -777,12 +822,28 @@ cudaError_t launch_one(const GemvArgs& a, const GemvPlan& p, cudaStream_t s) {
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    if (W4A16_GEMV_PDL) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    GemvArgs args = a;
+    if (a.cluster > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = static_cast<unsigned>(a.cluster);
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = n + 1;
+        // clusters only when all of them are resident at once; else tickets
+        if (!clusters_fit(reinterpret_cast<const void*>(kern), cfg, p.grid / a.cluster)) args.cluster = 0;
+        else ++n;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = W4A16_GEMV_PDL ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, kern, a);
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, kern, args);
 }
 
 template <bool kBf16, int MT, int COLS, bool kFact, bool kXPre = false, bool kMma = false>
@@ -858,6 +919,12 @@ constexpr double kStraddleCost = 2.0;
 // 4 / 2, 1x2048x2048 5.11 / 4.50 / 5.08 / 5.38, 4x1024x4096 6.17 / 5.91 /
 // 6.44 / 6.44.
 constexpr int kMinChunksPerCta = 8;
+// Largest cluster (portable size) whose CTAs sum a column block through
+// distributed shared memory instead of workspace slots and a ticket.
+#ifndef W4A16_GEMV_MAX_CLUSTER
+#define W4A16_GEMV_MAX_CLUSTER 8
+#endif
+constexpr int kMaxCluster = W4A16_GEMV_MAX_CLUSTER;
 
 // two partial slots (head and tail segment) per CTA, at most one CTA per SM
 size_t partial_region_bytes(const DeviceProps& dp) {
@@ -865,6 +932,48 @@ size_t partial_region_bytes(const DeviceProps& dp) {
 }
 
 namespace {
+
+// Never launched: a stand-in for the GEMV kernels (512 threads, one CTA per
+// SM) in the occupancy query below.
+__global__ void __launch_bounds__(kThreads, 1) cluster_probe_kernel() {}
+
+// How many clusters of `size` CTAs (one CTA per SM) the device holds at once;
+// asked once per device. It depends on how the SMs are grouped (a cluster
+// lives in one GPC): on a 152-SM GB300, 76 of 2, 46 of 3, 36 of 4, 23 of 6,
+// 15 of 7 or 8.
+int cluster_capacity(const DeviceProps& dp, int size) {
+    static std::mutex mu;
+    static std::map<int, std::array<int, kMaxCluster + 1>> cache;
+    if (size < 1 || size > kMaxCluster) return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(dp.device);
+    if (it == cache.end()) {
+        std::array<int, kMaxCluster + 1> cap{};
+        const void* k = reinterpret_cast<const void*>(cluster_probe_kernel);
+        if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(dp.smem_optin)) ==
+            cudaSuccess) {
+            for (int c = 1; c <= kMaxCluster; ++c) {
+                cudaLaunchConfig_t cfg = {};
+                cfg.gridDim = dim3(c);
+                cfg.blockDim = dim3(kThreads);
+                cfg.dynamicSmemBytes = dp.smem_optin;
+                cudaLaunchAttribute attr[1];
+                attr[0].id = cudaLaunchAttributeClusterDimension;
+                attr[0].val.clusterDim.x = static_cast<unsigned>(c);
+                attr[0].val.clusterDim.y = 1;
+                attr[0].val.clusterDim.z = 1;
+                cfg.attrs = attr;
+                cfg.numAttrs = 1;
+                int n = 0;
+                if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess) n = 0;
+                cap[c] = n;
+            }
+        }
+        (void)cudaGetLastError();
+        it = cache.emplace(dp.device, cap).first;
+    }
+    return it->second[size];
+}
 
 // `fact`: whether the kernel may apply zero-points through chunk sums of x
 // (the W4A16 layer for M <= 4; never for MXFP4 weights, which have none).
@@ -911,6 +1020,26 @@ GemvPlan plan(int M, int N, int K, bool fact, const DeviceProps& dp) {
             const double cost_sk = static_cast<double>(items) / (static_cast<double>(p.grid) * kWarps) + kStraddleCost;
             const double cost_al = static_cast<double>(items) / (static_cast<double>(aligned) * kWarps);
             if (cost_al < cost_sk) p.grid = static_cast<int>(aligned);
+        }
+        // A block-aligned grid of 2..8 CTAs per block sums each block in a
+        // cluster, if all its clusters can be resident at once. On a small
+        // layer (at most two chunks per warp) a grid of clusters that fit is
+        // taken even with fewer CTAs per block, down to half the grid: the
+        // cluster sum saves about 0.7 us (4x2048x2048: 5.23 -> 4.95 us with 96
+        // CTAs in clusters of 6 against 128 CTAs with tickets; 1x5376x21504
+        // with ~100 chunks a CTA: 14.56 -> 15.09 us with 126 CTAs, so not there).
+        p.cluster = 0;
+        if (sp >= 2 && sp <= kMaxCluster && p.grid == p.n_cb * sp && p.n_cb <= cluster_capacity(dp, sp))
+            p.cluster = static_cast<int>(sp);
+        if (!p.cluster) {
+            long long sc = std::min<long long>(std::min<long long>(want / p.n_cb, chunks / kMinChunksPerCta),
+                                               kMaxCluster);
+            while (sc >= 2 && p.n_cb > cluster_capacity(dp, static_cast<int>(sc))) --sc;
+            const long long gc = p.n_cb * sc;
+            if (sc >= 2 && 2 * gc >= p.grid && items <= gc * 2 * kWarps) {
+                p.grid = static_cast<int>(gc);
+                p.cluster = static_cast<int>(sc);
+            }
         }
     };
     size_grid(0);
@@ -974,6 +1103,7 @@ cudaError_t launch_gemv(const void* x, const uint32_t* qw, const void* sc, const
     a.g_shift = __builtin_ctz(static_cast<unsigned>(g));
     a.chunks = K / kChunk;
     a.items = plan.items;
+    a.cluster = plan.cluster;
     return bf16 ? launch_dtype<true>(a, plan, s) : launch_dtype<false>(a, plan, s);
 }
 
@@ -1001,6 +1131,7 @@ cudaError_t launch_mx_gemv(const void* x, const uint32_t* qw, const uint8_t* es,
     a.g_shift = __builtin_ctz(static_cast<unsigned>(mx::kBlock));
     a.chunks = K / kChunk;
     a.items = plan.items;
+    a.cluster = plan.cluster;
     return launch_mx_rows(a, plan, s);
 }
 

@@ -39,6 +39,7 @@ struct GemvPlan {
     long long items_split = 0;   // items of the blocks shared stream-K by all CTAs ([0, whole_first))
     int whole_first = 0;    // first of the blocks handed out whole
     int whole_per_cta = 0;  // whole blocks per CTA (after its stream-K share)
+    int cluster = 0;        // CTAs per column block summed through distributed shared memory (0: tickets)
     bool mma = false;       // products through warp-level tensor-core MMAs (W4A16, 2..16 rows)
     bool fact = false;      // zero-point applied per chunk through chunk sums of x
     bool xpre = false;      // with fact: the chunk sums computed once per CTA up front

@@ -275,6 +275,13 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
     return ok != 0;
 }
 
+// Load a 32-bit float from shared memory of cluster CTA `cta` at its local offset `addr`.
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr, uint32_t cta) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(map_to_cta(addr, cta)) : "memory");
+    return v;
+}
+
 // Store a 32-bit word to shared memory of cluster CTA `cta` at its local offset `addr`.
 __device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t cta, uint32_t v) {
     asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(map_to_cta(addr, cta)), "r"(v) : "memory");
