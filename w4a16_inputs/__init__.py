@@ -155,6 +155,9 @@ WORKLOADS = {w.name: w for w in [
     *[_w(f"gemv_4x{N}x{K}_g128_{a}_asym", "gemv", 4, N, K, 128, a, False)
       for a in ("f16", "bf16")
       for (N, K) in ((2048, 2048), (2048, 2560), (6144, 2048), (4096, 2048))],
+    # several decode rows on the gate_up shape (the GEMV's tensor-core MMA conversion)
+    _w("gemv_4x43008x5376_g32_f16_asym", "gemv", 4, 43008, 5376, 32, "f16", False),
+    _w("gemv_16x43008x5376_g32_bf16_asym", "gemv", 16, 43008, 5376, 32, "bf16", False),
     # qkv-like and down-like decode GEMV, g=32, bf16, symmetric and asymmetric
     *[_w(f"gemv_1x{N}x{K}_g32_bf16_{'sym' if s else 'asym'}", "gemv", 1, N, K, 32, "bf16", s)
       for (N, K) in ((16384, 5376), (5376, 21504)) for s in (True, False)],
