@@ -143,30 +143,63 @@ struct Act<true> {
 // contiguous bytes (no bank conflicts).
 __host__ __device__ constexpr int round128(int v) { return (v + 127) & ~127; }
 
+__host__ __device__ constexpr int group_width(int cols) { return cols < 4 ? cols : cols % 4 == 0 ? 4 : 3; }
+// A tensor copy moves at most 256 elements along a row: wider blocks arrive
+// as one copy per lane group (32 * W columns each).
+__host__ __device__ constexpr bool split_boxes(int cols) { return 32 * cols > 256; }
+__host__ __device__ constexpr int box_cols(int cols) { return split_boxes(cols) ? 32 * group_width(cols) : 32 * cols; }
+__host__ __device__ constexpr int scale_bytes(int cols) {
+    return split_boxes(cols) ? (cols / group_width(cols)) * round128(box_cols(cols) * 2) : round128(32 * cols * 2);
+}
+
 template <int COLS, int MT>
 struct Stage {
     static constexpr int CB = 32 * COLS;
-    static constexpr int W = COLS < 4 ? COLS : 4;         // columns per group
+    static constexpr int W = group_width(COLS);           // columns per group
     static constexpr int G = COLS / W;                    // groups per lane
+    static_assert(COLS % W == 0, "whole groups");
+    static constexpr bool kSplit = split_boxes(COLS);     // [G][4][32W] words, G scale rows
+    static constexpr int kBox = box_cols(COLS);
+    static constexpr int kSStride = kSplit ? round128(kBox * 2) : 0;   // bytes between the groups' scale rows
     // every block is a tensor-copy destination: 128-byte aligned
-    static constexpr int kQ = 0;                                          // [4][CB] uint32
-    static constexpr int kS = kQ + round128(kRowsPerChunk * CB * 4);      // [CB] 16-bit scales
-    static constexpr int kZ = kS + round128(CB * 2);                      // [CB / 8] uint32
+    static constexpr int kQ = 0;                                          // [4][CB] (or [G][4][kBox]) uint32
+    static constexpr int kS = kQ + round128(kRowsPerChunk * CB * 4);      // [CB] 16-bit scales (or G rows)
+    static constexpr int kZ = kS + scale_bytes(COLS);                     // [CB / 8] uint32
     static constexpr int kX = kZ + round128(CB / 2);                      // [MT][32] 16-bit x
     static constexpr int kBytes = kX + round128(MT * kChunk * 2);
-    static_assert(kS % 128 == 0 && kZ % 128 == 0 && kX % 128 == 0 && kBytes % 128 == 0,
+    static_assert(kS % 128 == 0 && kZ % 128 == 0 && kX % 128 == 0 && kBytes % 128 == 0 &&
+                      (kRowsPerChunk * kBox * 4) % 128 == 0,
                   "tensor-copy destinations must be 128-byte aligned");
     __device__ static int col(int lane, int gi, int u) { return gi * 32 * W + lane * W + u; }
+    // byte offsets of the lane's group gi: word row i, and its scales
+    __device__ static int q_off(int i, int lane, int gi) {
+        return kSplit ? kQ + gi * (kRowsPerChunk * kBox * 4) + i * kBox * 4 + lane * W * 4
+                      : kQ + i * CB * 4 + col(lane, gi, 0) * 4;
+    }
+    __device__ static int s_off(int lane, int gi) {
+        return kSplit ? kS + gi * kSStride + lane * W * 2 : kS + col(lane, gi, 0) * 2;
+    }
 };
 
 __host__ __device__ constexpr int stage_bytes(int cols, int mt) {
-    return round128(kRowsPerChunk * 32 * cols * 4) + round128(32 * cols * 2) + round128(32 * cols / 2) +
+    return round128(kRowsPerChunk * 32 * cols * 4) + scale_bytes(cols) + round128(32 * cols / 2) +
            round128(mt * kChunk * 2);
 }
 
 template <int BYTES>
 __device__ __forceinline__ void lds(uint32_t addr, uint32_t (&v)[(BYTES + 3) / 4]) {
-    if constexpr (BYTES == 16)
+    if constexpr (BYTES == 12) {   // three words, 4-byte aligned
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v[0]) : "r"(addr));
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v[1]) : "r"(addr + 4));
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v[2]) : "r"(addr + 8));
+    } else if constexpr (BYTES == 6) {   // three halves, 2-byte aligned: v[0] = h0 | h1 << 16, v[1] = h2
+        uint16_t h0, h1, h2;
+        asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h0) : "r"(addr));
+        asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h1) : "r"(addr + 2));
+        asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h2) : "r"(addr + 4));
+        v[0] = static_cast<uint32_t>(h0) | (static_cast<uint32_t>(h1) << 16);
+        v[1] = h2;
+    } else if constexpr (BYTES == 16)
         asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]) : "r"(addr));
     else if constexpr (BYTES == 8)
         asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v[0]), "=r"(v[1]) : "r"(addr));
@@ -303,8 +336,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
             const int c1 = static_cast<int>(std::min<long long>(chunks, c0 + (i_end - i_begin)));
             for (int j = 0, c = c0 + warp; j < kL2Prefetch && c < c1; ++j, c += kWarps) {
                 const int t = (c * kChunk) >> g_shift;
-                tma_prefetch_l2_2d(&a.tq, cb * CB, c * kRowsPerChunk);
-                tma_prefetch_l2_2d(&a.ts, cb * CB, t);
+#pragma unroll
+                for (int gi = 0; gi < (St::kSplit ? G : 1); ++gi) {
+                    tma_prefetch_l2_2d(&a.tq, cb * CB + gi * St::kBox, c * kRowsPerChunk);
+                    tma_prefetch_l2_2d(&a.ts, cb * CB + gi * St::kBox, t);
+                }
                 if constexpr (kZBulk) tma_prefetch_l2_2d(&a.tz, cb * (CB / 8), t);
             }
         }
@@ -358,8 +394,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
             constexpr uint32_t kBytes =
                 kRowsPerChunk * CB * 4 + (kMx ? CB : CB * 2) + (kZBulk ? CB / 2 : 0) + MT * kChunk * 2;
             mbar_arrive_expect_tx(bar, kBytes);
-            tma_load_2d(base + St::kQ, &a.tq, cb * CB, c * kRowsPerChunk, bar);
-            tma_load_2d(base + St::kS, &a.ts, cb * CB, t, bar);
+            if constexpr (St::kSplit) {
+#pragma unroll
+                for (int gi = 0; gi < G; ++gi) {
+                    tma_load_2d(base + St::kQ + gi * (kRowsPerChunk * St::kBox * 4), &a.tq, cb * CB + gi * St::kBox,
+                                c * kRowsPerChunk, bar);
+                    tma_load_2d(base + St::kS + gi * St::kSStride, &a.ts, cb * CB + gi * St::kBox, t, bar);
+                }
+            } else {
+                tma_load_2d(base + St::kQ, &a.tq, cb * CB, c * kRowsPerChunk, bar);
+                tma_load_2d(base + St::kS, &a.ts, cb * CB, t, bar);
+            }
             if constexpr (kZBulk) tma_load_2d(base + St::kZ, &a.tz, cb * (CB / 8), t, bar);
             tma_load_2d(base + St::kX, &a.tx, c * kChunk, 0, bar);
         };
@@ -391,7 +436,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
                 __syncwarp();
             }
             // scales and zero-points of the lane's columns
-            uint32_t sw[G][(2 * W + 3) / 4], zw[G];
+            // zw: the zero-point word of the group's first column; zw2: of its last
+            // (a 3-column group can cross a word)
+            uint32_t sw[G][(2 * W + 3) / 4], zw[G], zw2[G];
 #pragma unroll
             for (int gi = 0; gi < G; ++gi) {
                 const int c0l = St::col(lane, gi, 0);
@@ -400,24 +447,44 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
                     lds<W>(base + St::kS + c0l, e);
                     sw[gi][0] = e[0];
                 } else
-                    lds<2 * W>(base + St::kS + c0l * 2, sw[gi]);
+                    lds<2 * W>(base + St::s_off(lane, gi), sw[gi]);
                 if constexpr (!kSym) {
+                    const int c1l = c0l + W - 1;
                     if constexpr (kZBulk) {
                         uint32_t v[1];
                         lds<4>(base + St::kZ + (c0l >> 3) * 4, v);
                         zw[gi] = v[0];
+                        if constexpr (W == 3) {
+                            lds<4>(base + St::kZ + (c1l >> 3) * 4, v);
+                            zw2[gi] = v[0];
+                        } else {
+                            zw2[gi] = zw[gi];
+                        }
                     } else {
                         const int t = (c * kChunk) >> g_shift;
-                        const int n = cb * CB + c0l;
-                        zw[gi] = n < N ? __ldg(a.qz + static_cast<size_t>(t) * (N >> 3) + (n >> 3)) : 0u;
+                        const int n = cb * CB + c0l, n1 = cb * CB + c1l;
+                        const uint32_t* zr = a.qz + static_cast<size_t>(t) * (N >> 3);
+                        zw[gi] = n < N ? __ldg(zr + (n >> 3)) : 0u;
+                        if constexpr (W == 3)
+                            zw2[gi] = n1 < N ? __ldg(zr + (n1 >> 3)) : 0u;
+                        else
+                            zw2[gi] = zw[gi];
                     }
                 } else {
                     zw[gi] = 0u;
+                    zw2[gi] = 0u;
                 }
             }
             auto zval = [&](int j) -> uint32_t {
                 const int gi = j / W, u = j % W;
-                return kSym ? 8u : ((zw[gi] >> (4 * ((St::col(lane, gi, 0) & 7) + u))) & 0xFu);
+                if constexpr (kSym) return 8u;
+                if constexpr (W == 3) {
+                    const int cl = St::col(lane, gi, 0), cu = cl + u;
+                    const uint32_t w = (cu >> 3) == (cl >> 3) ? zw[gi] : zw2[gi];
+                    return (w >> (4 * (cu & 7))) & 0xFu;
+                } else {
+                    return (zw[gi] >> (4 * ((St::col(lane, gi, 0) & 7) + u))) & 0xFu;
+                }
             };
             auto sval = [&](int j) -> float {
                 const int gi = j / W, u = j % W;
@@ -487,7 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
 #pragma unroll
                 for (int gi = 0; gi < G; ++gi) {
                     uint32_t v[W];
-                    lds<4 * W>(base + St::kQ + i * CB * 4 + St::col(lane, gi, 0) * 4, v);
+                    lds<4 * W>(base + St::q_off(i, lane, gi), v);
 #pragma unroll
                     for (int u = 0; u < W; ++u) q[gi * W + u] = v[u];
                 }
@@ -865,7 +932,9 @@ cudaError_t launch_dtype(const GemvArgs& a, const GemvPlan& p, cudaStream_t s) {
     }
     if (p.fact && p.xpre) {
         switch (p.mt) {
-            case 1: return launch_sym<kBf16, 1, 8, true, true>(a, p, s);
+            case 1:
+                return p.cols == 9 ? launch_sym<kBf16, 1, 9, true, true>(a, p, s)
+                                   : launch_sym<kBf16, 1, 8, true, true>(a, p, s);
             case 2: return launch_sym<kBf16, 2, 4, true, true>(a, p, s);
             case 3: return launch_sym<kBf16, 3, 4, true, true>(a, p, s);
             case 4: return launch_sym<kBf16, 4, 4, true, true>(a, p, s);
@@ -874,7 +943,8 @@ cudaError_t launch_dtype(const GemvArgs& a, const GemvPlan& p, cudaStream_t s) {
     }
     if (p.fact) {
         switch (p.mt) {
-            case 1: return launch_sym<kBf16, 1, 8, true>(a, p, s);
+            case 1:
+                return p.cols == 9 ? launch_sym<kBf16, 1, 9, true>(a, p, s) : launch_sym<kBf16, 1, 8, true>(a, p, s);
             case 2: return launch_sym<kBf16, 2, 4, true>(a, p, s);
             case 3: return launch_sym<kBf16, 3, 4, true>(a, p, s);
             case 4: return launch_sym<kBf16, 4, 4, true>(a, p, s);
@@ -987,8 +1057,14 @@ GemvPlan plan(int M, int N, int K, bool fact, const DeviceProps& dp) {
     } else {
         p.mt = M <= 1 ? 1 : M <= 2 ? 2 : M <= 3 ? 3 : M <= 4 ? 4 : M <= 6 ? 6 : M <= 8 ? 8 : M <= 12 ? 12 : 16;
         p.cols = p.mt == 1 ? 8 : p.mt <= 4 ? 4 : p.mt <= 8 ? 2 : 1;
+        // One row: when 256-column blocks outnumber the SMs but 288-column
+        // blocks do not (43008 columns: 168 against 150 blocks on 152 SMs),
+        // 9 columns a lane let every CTA own one whole block: no split-K fix-up
+        // and no block boundary inside a CTA's range.
+        if (p.mt == 1 && fact && (N + 255) / 256 > dp.sms && (N + 287) / 288 <= dp.sms) p.cols = 9;
     }
     p.cb = 32 * p.cols;
+    p.box_cols = box_cols(p.cols);
     p.n_cb = (N + p.cb - 1) / p.cb;
     p.warps = kWarps;
     const int chunks = K / kChunk;
@@ -1078,9 +1154,10 @@ cudaError_t launch_gemv(const void* x, const uint32_t* qw, const void* sc, const
     GemvArgs a;
     const CUtensorMapDataType act = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     const uint32_t cb = static_cast<uint32_t>(plan.cb);
-    if (!encode_2d(&a.tq, CU_TENSOR_MAP_DATA_TYPE_INT32, qw, (uint64_t)N, (uint64_t)(K / 8), (uint64_t)N * 4, cb,
+    const uint32_t box = static_cast<uint32_t>(plan.box_cols);   // cb, or one lane group's columns
+    if (!encode_2d(&a.tq, CU_TENSOR_MAP_DATA_TYPE_INT32, qw, (uint64_t)N, (uint64_t)(K / 8), (uint64_t)N * 4, box,
                    kRowsPerChunk, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !encode_2d(&a.ts, act, sc, (uint64_t)N, (uint64_t)(K / g), (uint64_t)N * 2, cb, 1,
+        !encode_2d(&a.ts, act, sc, (uint64_t)N, (uint64_t)(K / g), (uint64_t)N * 2, box, 1,
                    CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !encode_2d(&a.tx, act, x, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, kChunk, plan.mt,
                    CU_TENSOR_MAP_SWIZZLE_NONE))

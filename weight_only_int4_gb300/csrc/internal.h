@@ -32,6 +32,7 @@ struct GemvPlan {
     int mt = 0;             // row template (>= M)
     int cols = 0;           // columns per lane
     int cb = 0;             // columns per column block (32 * cols)
+    int box_cols = 0;       // columns per tensor copy of weights and scales (cb, or 96 for 288-column blocks)
     int n_cb = 0;           // column blocks
     int warps = 0;          // warps per CTA (streaming warps + one reduction warp)
     int grid = 0;           // persistent CTAs (one per SM at most)
