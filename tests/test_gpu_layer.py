@@ -45,6 +45,19 @@ def test_gemv_parity(act, g, sym, M):
         parity("gemv", M, N, K, g, act, sym, seed=M + N + K)
 
 
+# One row with more 256-column blocks than SMs but at most one 288-column block
+# per SM: 9 columns a lane, three 96-column tensor copies per row set, every CTA
+# one whole block. Ragged last block, N % 32 != 0 (zero-point words read per
+# lane; a lane's 3-column group can cross a word), and N = 152 x 288.
+WIDE_BLOCK_LAYERS = [(43000, 512, 128, "f16", False), (39936, 256, 32, "bf16", True),
+                     (43776, 256, 64, "f16", False), (42024, 384, 32, "bf16", False)]
+
+
+@pytest.mark.parametrize("N,K,g,act,sym", WIDE_BLOCK_LAYERS)
+def test_gemv_wide_blocks(N, K, g, act, sym):
+    parity("gemv", 1, N, K, g, act, sym, seed=N + K)
+
+
 # Layers just above 4 Mi weights: 2..16 rows run the GEMV's tensor-core MMA
 # conversion (smaller layers keep FP32 FMAs up to 8 rows). One with N % 32 != 0
 # (zero-point words read per lane, ragged last column block), one with N % 32 == 0
