@@ -59,7 +59,7 @@ def test_gemv_wide_blocks(N, K, g, act, sym):
 
 
 # Layers just above 4 Mi weights: 2..16 rows run the GEMV's tensor-core MMA
-# conversion (smaller layers keep FP32 FMAs up to 8 rows). One with N % 32 != 0
+# conversion (smaller layers keep FP32 FMAs up to 2 rows). One with N % 32 != 0
 # (zero-point words read per lane, ragged last column block), one with N % 32 == 0
 # (zero-point words by tensor copy).
 MMA_LAYERS = [(2056, 2304), (2304, 2048)]
@@ -306,12 +306,13 @@ def test_binding_rejections():
 
 @pytest.mark.parametrize("M,N,K,g,act", [(5, 16392, 4096, 32, "f16"), (8, 9216, 4096, 128, "bf16"),
                                          (16, 2056, 5120, 64, "f16"), (12, 43008, 640, 32, "bf16"),
-                                         (2, 4104, 4096, 64, "bf16"), (7, 776, 8192, 128, "f16")])
+                                         (2, 4104, 4096, 64, "bf16"), (7, 776, 8192, 128, "f16"),
+                                         (3, 10248, 4352, 64, "bf16"), (8, 41000, 1280, 128, "f16")])
 def test_gemv_mma_rows(M, N, K, g, act):
-    """2..16 rows of layers above 4 Mi weights go through the GEMV's
-    tensor-core MMA conversion (8 x-rows x 128 columns up to M = 8, 16 x 64
-    above; ragged column blocks included): parity with the oracle, and two
-    calls bit-identical."""
+    """3..16 rows (2 rows above 4 Mi weights) go through the GEMV's tensor-core
+    MMA conversion: 8 x-rows x 64 columns up to 40 Mi weights, x 128 columns
+    above (the last two cases), 16 x 64 from M = 9; ragged column blocks
+    included. Parity with the oracle, and two calls bit-identical."""
     dc = DeviceCase(make_case(M, N, K, g, act, False, seed=M * 3 + g))
     need = w4.workspace_bytes(w4.OP_GEMV, M, N, K, g)
     assert need > w4.workspace_bytes(w4.OP_GEMM, M, N, K, g)   # both kernels' partial regions

@@ -98,11 +98,17 @@ constexpr int kFactMaxM = 4;          // zero-point through the chunk's sum of x
 #endif
 constexpr int kMmaMinM = W4A16_GEMV_MMA_MIN_M;
 // ... except layers of at most kFmaSmallMaxWeights weights with at most
-// kFmaSmallMaxM rows, which stay on FP32 FMAs (measured at 2048 x 2048: M=4
-// 4.98 against 5.13 us, M=8 5.91 against 6.39 us; at 2048 x 2560 and above the
-// MMA conversion wins or ties).
-constexpr int kFmaSmallMaxM = 8;
+// kFmaSmallMaxM rows, which stay on FP32 FMAs (2048 x 2048, M = 2: 4.03 us
+// against 4.24 with MMAs; from M = 3 the MMA conversion wins: 4.39 -> 4.32).
+constexpr int kFmaSmallMaxM = 2;
 constexpr long long kFmaSmallMaxWeights = 4ll << 20;
+// The 8-row MMA template takes 64-column blocks (not 128) on layers of at
+// most this many weights: twice the blocks, so on a small layer all 16 warps
+// of more CTAs get a chunk (4x2048x2048 4.94 -> 4.36 us, 4x6144x2048 6.74 ->
+// 5.80, 8x8192x4096 9.78 -> 8.21); from 84 Mi weights on the narrower chunks'
+// per-column overheads lose (4x16384x5376 15.8 -> 21.2, 4x43008x5376 40.2 ->
+// 45.6).
+constexpr long long kMmaNarrowMaxWeights = 40ll << 20;
 constexpr int kXPreMinChunksPerWarp = 8;
 constexpr size_t kXsumSmemLimit = 32 * 1024;
 constexpr unsigned long long kWaitLimitCycles = 4000000000ull;   // ~2 s at 2 GHz
@@ -289,8 +295,8 @@ template <bool kBf16, int MT, int COLS, bool kSym, bool kFact, bool kZBulk, bool
           bool kMma = false>
 __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant__ GemvArgs a) {
     static_assert(!kXPre || kFact, "precomputed chunk sums serve the zero-point factorisation");
-    static_assert(!kMma || (!kMx && !kFact && ((MT == 8 && COLS == 4) || (MT == 16 && COLS == 2))),
-                  "MMA conversion: 8 rows x 128 columns or 16 rows x 64 columns, zero-points per nibble pair");
+    static_assert(!kMma || (!kMx && !kFact && ((MT == 8 && (COLS == 4 || COLS == 2)) || (MT == 16 && COLS == 2))),
+                  "MMA conversion: 8 rows x 128 or 64 columns, 16 rows x 64 columns, zero-points per nibble pair");
     static_assert(!kMx || (kBf16 && kSym && !kFact && !kZBulk), "MXFP4: bf16, no zero-points");
     static_assert(!kMx || Stage<COLS, MT>::kX - Stage<COLS, MT>::kZ >= 4 * MT, "row factors fit the zero-point block");
     using A = Act<kBf16>;
@@ -925,7 +931,9 @@ template <bool kBf16>
 cudaError_t launch_dtype(const GemvArgs& a, const GemvPlan& p, cudaStream_t s) {
     if (p.mma) {
         switch (p.mt) {
-            case 8: return launch_sym<kBf16, 8, 4, false, false, true>(a, p, s);
+            case 8:
+                return p.cols == 2 ? launch_sym<kBf16, 8, 2, false, false, true>(a, p, s)
+                                   : launch_sym<kBf16, 8, 4, false, false, true>(a, p, s);
             case 16: return launch_sym<kBf16, 16, 2, false, false, true>(a, p, s);
             default: return cudaErrorInvalidValue;
         }
@@ -1054,6 +1062,7 @@ GemvPlan plan(int M, int N, int K, bool fact, const DeviceProps& dp) {
     if (p.mma) {
         p.mt = M <= 8 ? 8 : 16;
         p.cols = M <= 8 ? 4 : 2;
+        if (p.mt == 8 && static_cast<long long>(N) * K <= kMmaNarrowMaxWeights) p.cols = 2;
     } else {
         p.mt = M <= 1 ? 1 : M <= 2 ? 2 : M <= 3 ? 3 : M <= 4 ? 4 : M <= 6 ? 6 : M <= 8 ? 8 : M <= 12 ? 12 : 16;
         p.cols = p.mt == 1 ? 8 : p.mt <= 4 ? 4 : p.mt <= 8 ? 2 : 1;
