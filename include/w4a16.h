@@ -130,7 +130,7 @@ size_t w4a16_workspace_bytes(w4a16_op op, int64_t M, int64_t N, int64_t K, int64
 /*
  * w4a16_gemv -- decode path, 1 <= M <= 16.
  *
- * One row (and up to 8 rows of a layer of at most 4 * 2^20 weights) is
+ * One row (and two rows of a layer of at most 4 * 2^20 weights) is
  * converted with FP32 FMAs; 2..16 rows otherwise go through warp-level
  * m16n8k16 tensor-core MMAs: (q - z) formed exactly in 16 bits as the A
  * operand, x as B, FP32 accumulators scaled once per 32-row chunk (measured
