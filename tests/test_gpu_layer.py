@@ -310,8 +310,9 @@ def test_binding_rejections():
                                          (3, 10248, 4352, 64, "bf16"), (8, 41000, 1280, 128, "f16")])
 def test_gemv_mma_rows(M, N, K, g, act):
     """3..16 rows (2 rows above 4 Mi weights) go through the GEMV's tensor-core
-    MMA conversion: 8 x-rows x 64 columns up to 40 Mi weights, x 128 columns
-    above (the last two cases), 16 x 64 from M = 9; ragged column blocks
+    MMA conversion: 8 x-rows x 64 columns where those blocks give a
+    block-aligned grid, x 128 columns otherwise (the last two cases: more
+    narrow blocks than SMs), 16 x 64 from M = 9; ragged column blocks
     included. Parity with the oracle, and two calls bit-identical."""
     dc = DeviceCase(make_case(M, N, K, g, act, False, seed=M * 3 + g))
     need = w4.workspace_bytes(w4.OP_GEMV, M, N, K, g)

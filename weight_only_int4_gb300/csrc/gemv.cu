@@ -102,13 +102,7 @@ constexpr int kMmaMinM = W4A16_GEMV_MMA_MIN_M;
 // against 4.24 with MMAs; from M = 3 the MMA conversion wins: 4.39 -> 4.32).
 constexpr int kFmaSmallMaxM = 2;
 constexpr long long kFmaSmallMaxWeights = 4ll << 20;
-// The 8-row MMA template takes 64-column blocks (not 128) on layers of at
-// most this many weights: twice the blocks, so on a small layer all 16 warps
-// of more CTAs get a chunk (4x2048x2048 4.94 -> 4.36 us, 4x6144x2048 6.74 ->
-// 5.80, 8x8192x4096 9.78 -> 8.21); from 84 Mi weights on the narrower chunks'
-// per-column overheads lose (4x16384x5376 15.8 -> 21.2, 4x43008x5376 40.2 ->
-// 45.6).
-constexpr long long kMmaNarrowMaxWeights = 40ll << 20;
+
 constexpr int kXPreMinChunksPerWarp = 8;
 constexpr size_t kXsumSmemLimit = 32 * 1024;
 constexpr unsigned long long kWaitLimitCycles = 4000000000ull;   // ~2 s at 2 GHz
@@ -1055,14 +1049,14 @@ int cluster_capacity(const DeviceProps& dp, int size) {
 
 // `fact`: whether the kernel may apply zero-points through chunk sums of x
 // (the W4A16 layer for M <= 4; never for MXFP4 weights, which have none).
-GemvPlan plan(int M, int N, int K, bool fact, const DeviceProps& dp) {
+// `narrow`: the 8-row MMA template with 64-column blocks instead of 128.
+GemvPlan plan_cols(int M, int N, int K, bool fact, const DeviceProps& dp, bool narrow) {
     GemvPlan p;
     p.mma = fact && M >= kMmaMinM &&
             (M > kFmaSmallMaxM || static_cast<long long>(N) * K > kFmaSmallMaxWeights);
     if (p.mma) {
         p.mt = M <= 8 ? 8 : 16;
-        p.cols = M <= 8 ? 4 : 2;
-        if (p.mt == 8 && static_cast<long long>(N) * K <= kMmaNarrowMaxWeights) p.cols = 2;
+        p.cols = M <= 8 && !narrow ? 4 : 2;
     } else {
         p.mt = M <= 1 ? 1 : M <= 2 ? 2 : M <= 3 ? 3 : M <= 4 ? 4 : M <= 6 ? 6 : M <= 8 ? 8 : M <= 12 ? 12 : 16;
         p.cols = p.mt == 1 ? 8 : p.mt <= 4 ? 4 : p.mt <= 8 ? 2 : 1;
@@ -1143,6 +1137,19 @@ GemvPlan plan(int M, int N, int K, bool fact, const DeviceProps& dp) {
     // sums over one another's tickets.
     p.partial_bytes = partial_region_bytes(dp);
     p.device = dp.device;
+    return p;
+}
+
+// The 8-row MMA template takes 64-column blocks when they give a
+// block-aligned grid (whole blocks or a whole number of CTAs per block), else
+// 128-column blocks. Narrow blocks double the blocks, so more warps of more
+// CTAs get chunks (aligned, us, 64 vs 128 columns: 4x2048x2048 4.37 / 5.12,
+// 4x6144x2048 5.75 / 6.72, 8x2048x8192 6.92 / 8.64, 8x8192x4096 8.23 / 9.79);
+// a stream-K grid of narrow blocks loses (3x5376x5376 11.5 / 8.9, 4x14336x2048
+// 12.8 / 8.1), and more narrow blocks than SMs never align.
+GemvPlan plan(int M, int N, int K, bool fact, const DeviceProps& dp) {
+    GemvPlan p = plan_cols(M, N, K, fact, dp, true);
+    if (p.mma && p.mt == 8 && p.grid % p.n_cb != 0) p = plan_cols(M, N, K, fact, dp, false);
     return p;
 }
 
