@@ -1,15 +1,18 @@
 """Decode GEMV parity with skewed, mostly positive activations.
 
-For M <= 4 the GEMV applies the zero-point once per 32-row chunk through the
-chunk's sum of x: sum (q - z) x = sum (magic + q) x - (magic + z) sum x, a
-difference of two FP32 sums far larger than the result. Zero-mean x keeps the
+For one row (and two rows of a layer of at most 4 Mi weights) the GEMV applies
+the zero-point once per 32-row chunk through the chunk's sum of x:
+sum (q - z) x = sum (magic + q) x - (magic + z) sum x, a difference of two FP32
+sums far larger than the result; more rows go through tensor-core MMAs on the
+exact (q - z), whose FP32 accumulation meets the same x. Zero-mean x keeps the
 chunk sums small; activations after SiLU or GELU are mostly positive, which
 makes them, and the cancellation, largest. "qsa_prompt_attn: Q4_0 KV on tensor
 cores" (§Measured, "A bug the tests caught") records a real bug that a narrow
 input distribution hid. These cases draw x = 4 + N(0, 1) and x = 3 |N(0, 1)|
 on the decode shapes of "Keep W4A16 zero-points packed at 4 bits instead of
-expanding to 2 bytes" (§Results: gate_up, qkv, down) and compare every output
-of M = 1..4 with the FP64 oracle at the parity tolerance.
+expanding to 2 bytes" (§Results: gate_up, qkv, down) and on two small layers,
+and compare every output of M = 1..4 with the FP64 oracle at the parity
+tolerance.
 """
 import pytest
 
@@ -27,6 +30,9 @@ SHAPES = {
     "down_bf16": (5376, 21504, 32, "bf16", False),
     "down_bf16_sym": (5376, 21504, 32, "bf16", True),
     "g128_f16": (6144, 2048, 128, "f16", False),
+    # at most 4 Mi weights: two rows stay on the factorised FMA path
+    "small_f16": (2048, 2048, 128, "f16", False),
+    "small_bf16_sym": (2048, 1536, 64, "bf16", True),
 }
 
 

@@ -129,6 +129,22 @@ def test_mx_gemv_activation_range(M, spread):
     assert_close(y, d.reference(), (M, spread))
 
 
+@pytest.mark.parametrize("N,K", [(42992, 512), (39936, 256)])
+def test_mx_gemv_wide_blocks(N, K):
+    """One row with more 256-column blocks than SMs but at most one 288-column
+    block per SM: 9 columns a lane, three 96-column copies of the words and of
+    the exponent bytes per chunk, every CTA one whole block (42992: ragged last
+    block)."""
+    case = make_mx_case(1, N, K, seed=N + K)
+    d = MxDevice(case)
+    buf, y, pad = guarded_out(1, N, torch.bfloat16)
+    w4.mxfp4_gemv(d.x, d.qw, d.e, out=y)
+    torch.cuda.synchronize()
+    check_guards(buf, pad)
+    assert_close(y, d.reference(), (1, N, K))
+    assert w4.device_status() == w4.OK
+
+
 @pytest.mark.parametrize("M,N,K", [(16, 10256, 1024), (8, 43008, 896)])
 def test_mx_gemv_tensor_core_rows(M, N, K):
     """Rows of a layer above the hand-over threshold (10 Mi weights at 13..16

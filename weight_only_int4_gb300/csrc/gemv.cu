@@ -176,8 +176,10 @@ struct Stage {
         return kSplit ? kQ + gi * (kRowsPerChunk * kBox * 4) + i * kBox * 4 + lane * W * 4
                       : kQ + i * CB * 4 + col(lane, gi, 0) * 4;
     }
-    __device__ static int s_off(int lane, int gi) {
-        return kSplit ? kS + gi * kSStride + lane * W * 2 : kS + col(lane, gi, 0) * 2;
+    // `bytes`: 2 for 16-bit scales, 1 for MXFP4 exponent bytes (whose rows fit
+    // the same slots)
+    __device__ static int s_off(int lane, int gi, int bytes = 2) {
+        return kSplit ? kS + gi * kSStride + lane * W * bytes : kS + col(lane, gi, 0) * bytes;
     }
 };
 
@@ -192,6 +194,12 @@ __device__ __forceinline__ void lds(uint32_t addr, uint32_t (&v)[(BYTES + 3) / 4
         asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v[0]) : "r"(addr));
         asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v[1]) : "r"(addr + 4));
         asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v[2]) : "r"(addr + 8));
+    } else if constexpr (BYTES == 3) {   // three bytes: v[0] = b0 | b1 << 8 | b2 << 16
+        uint16_t b0, b1, b2;
+        asm volatile("ld.shared.u8 %0, [%1];" : "=h"(b0) : "r"(addr));
+        asm volatile("ld.shared.u8 %0, [%1];" : "=h"(b1) : "r"(addr + 1));
+        asm volatile("ld.shared.u8 %0, [%1];" : "=h"(b2) : "r"(addr + 2));
+        v[0] = static_cast<uint32_t>(b0) | (static_cast<uint32_t>(b1) << 8) | (static_cast<uint32_t>(b2) << 16);
     } else if constexpr (BYTES == 6) {   // three halves, 2-byte aligned: v[0] = h0 | h1 << 16, v[1] = h2
         uint16_t h0, h1, h2;
         asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h0) : "r"(addr));
@@ -444,7 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
                 const int c0l = St::col(lane, gi, 0);
                 if constexpr (kMx) {
                     uint32_t e[1];   // the W exponent bytes of the group
-                    lds<W>(base + St::kS + c0l, e);
+                    lds<W>(base + St::s_off(lane, gi, 1), e);
                     sw[gi][0] = e[0];
                 } else
                     lds<2 * W>(base + St::s_off(lane, gi), sw[gi]);
@@ -968,7 +976,9 @@ cudaError_t launch_dtype(const GemvArgs& a, const GemvPlan& p, cudaStream_t s) {
 
 cudaError_t launch_mx_rows(const GemvArgs& a, const GemvPlan& p, cudaStream_t s) {
     switch (p.mt) {
-        case 1: return launch_one<true, 1, 8, true, false, false, true>(a, p, s);
+        case 1:
+            return p.cols == 9 ? launch_one<true, 1, 9, true, false, false, true>(a, p, s)
+                               : launch_one<true, 1, 8, true, false, false, true>(a, p, s);
         case 2: return launch_one<true, 2, 4, true, false, false, true>(a, p, s);
         case 3: return launch_one<true, 3, 4, true, false, false, true>(a, p, s);
         case 4: return launch_one<true, 4, 4, true, false, false, true>(a, p, s);
@@ -1064,7 +1074,7 @@ GemvPlan plan_cols(int M, int N, int K, bool fact, const DeviceProps& dp, bool n
         // blocks do not (43008 columns: 168 against 150 blocks on 152 SMs),
         // 9 columns a lane let every CTA own one whole block: no split-K fix-up
         // and no block boundary inside a CTA's range.
-        if (p.mt == 1 && fact && (N + 255) / 256 > dp.sms && (N + 287) / 288 <= dp.sms) p.cols = 9;
+        if (p.mt == 1 && (N + 255) / 256 > dp.sms && (N + 287) / 288 <= dp.sms) p.cols = 9;
     }
     p.cb = 32 * p.cols;
     p.box_cols = box_cols(p.cols);
@@ -1204,11 +1214,11 @@ cudaError_t launch_mx_gemv(const void* x, const uint32_t* qw, const uint8_t* es,
                            const GemvPlan& plan, float* partials, uint32_t* tickets, cudaStream_t s) {
     if (plan.fact) return cudaErrorInvalidValue;   // the plan must come from plan_mx_gemv
     GemvArgs a;
-    const uint32_t cb = static_cast<uint32_t>(plan.cb);
-    if (!encode_2d(&a.tq, CU_TENSOR_MAP_DATA_TYPE_INT32, qw, (uint64_t)N, (uint64_t)(K / 8), (uint64_t)N * 4, cb,
+    const uint32_t box = static_cast<uint32_t>(plan.box_cols);   // cb, or one lane group's columns
+    if (!encode_2d(&a.tq, CU_TENSOR_MAP_DATA_TYPE_INT32, qw, (uint64_t)N, (uint64_t)(K / 8), (uint64_t)N * 4, box,
                    kRowsPerChunk, CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !encode_2d(&a.ts, CU_TENSOR_MAP_DATA_TYPE_UINT8, es, (uint64_t)N, (uint64_t)(K / mx::kBlock), (uint64_t)N,
-                   cb, 1, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+                   box, 1, CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !encode_2d(&a.tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, kChunk,
                    plan.mt, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
