@@ -306,12 +306,15 @@ w4a16_status w4a16_mxfp4_dequant(const int32_t* qweight, const uint8_t* escale, 
  * w4a16_mxfp4_gemv -- decode path for MXFP4 weights, 1 <= M <= 16: the
  * w4a16_gemv kernel with the E2M1 decode in place of the 4-bit integer one
  * (each 32-row chunk is one exponent block; its scale 2^(e - 127) is applied
- * in FP32 once per chunk) and FP32 FMAs for every M. Same persistent grid,
- * deterministic fix-up and programmatic launch. 5..16 rows of a large enough
- * layer run the few-row tensor-core kernel of w4a16_mxfp4_gemm instead:
- * N * K >= 64 * 2^20 weights for M = 5..6, 36 * 2^20 for M = 7..8, 24 * 2^20
- * for M = 9..12 and 10 * 2^20 for M = 13..16 (where the FMA conversion,
- * 8 * M products per packed word, falls behind).
+ * in FP32 once per chunk). Same persistent grid, deterministic fix-up and
+ * programmatic launch, and the same conversion choice: FP32 FMAs for one row
+ * (and two rows of a layer of at most 4 * 2^20 weights), warp-level
+ * tensor-core MMAs on fp16 operands otherwise (each chunk's x rows are first
+ * rescaled to fp16 by a power of two per row, undone in FP32). 9..16 rows of
+ * a layer with at least 48 * 2^20 weights run the few-row tensor-core kernel
+ * of w4a16_mxfp4_gemm instead, where the 16-row rescale costs more than the
+ * MMAs save (43008 x 5376, M = 12: 110.5 against 77.3 us; M = 8 stays on the
+ * GEMV: 59.4 against 77.1 us).
  * Workspace: at least w4a16_workspace_bytes(W4A16_OP_GEMV, M, N, K, 32) bytes,
  * with the same ownership and zero-fill rules as for w4a16_gemv.
  */

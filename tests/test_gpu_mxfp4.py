@@ -145,11 +145,12 @@ def test_mx_gemv_wide_blocks(N, K):
     assert w4.device_status() == w4.OK
 
 
-@pytest.mark.parametrize("M,N,K", [(16, 10256, 1024), (8, 43008, 896)])
+@pytest.mark.parametrize("M,N,K", [(16, 10256, 1024), (8, 43008, 896), (12, 43008, 1280), (3, 4112, 2048)])
 def test_mx_gemv_tensor_core_rows(M, N, K):
-    """Rows of a layer above the hand-over threshold (10 Mi weights at 13..16
-    rows, 36 Mi at 7..8) run the few-row tensor-core kernel: parity with the
-    oracle, guards intact, two calls bit-identical."""
+    """2..16 rows: the GEMV's MMA conversion on fp16-rescaled x (10 and 37 Mi
+    weights, 3 rows of 8 Mi), and 12 rows of a 52.5 Mi layer, above the
+    hand-over to the few-row tensor-core kernel (9..16 rows, 48 Mi weights):
+    parity with the oracle, guards intact, two calls bit-identical."""
     case = make_mx_case(M, N, K, seed=M + N)
     d = MxDevice(case)
     buf, y, pad = guarded_out(M, N, torch.bfloat16)

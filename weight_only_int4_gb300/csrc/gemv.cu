@@ -297,7 +297,7 @@ template <bool kBf16, int MT, int COLS, bool kSym, bool kFact, bool kZBulk, bool
           bool kMma = false>
 __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant__ GemvArgs a) {
     static_assert(!kXPre || kFact, "precomputed chunk sums serve the zero-point factorisation");
-    static_assert(!kMma || (!kMx && !kFact && ((MT == 8 && (COLS == 4 || COLS == 2)) || (MT == 16 && COLS == 2))),
+    static_assert(!kMma || (!kFact && ((MT == 8 && (COLS == 4 || COLS == 2)) || (MT == 16 && COLS == 2))),
                   "MMA conversion: 8 rows x 128 or 64 columns, 16 rows x 64 columns, zero-points per nibble pair");
     static_assert(!kMx || (kBf16 && kSym && !kFact && !kZBulk), "MXFP4: bf16, no zero-points");
     static_assert(!kMx || Stage<COLS, MT>::kX - Stage<COLS, MT>::kZ >= 4 * MT, "row factors fit the zero-point block");
@@ -417,32 +417,35 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
             tma_load_2d(base + St::kX, &a.tx, c * kChunk, 0, bar);
         };
 
+        // kMx: lane l rescales x[m][l] of every row m < M of the stage's x
+        // slice to fp16 in place; the rows' factors 2^-c go to the stage's
+        // zero-point block, unused without zero-points
+        auto mx_rescale = [&](uint32_t base) {
+            uint16_t xb[MT];
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                xb[m] = 0;
+                if (m < M)
+                    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(xb[m]) : "r"(base + St::kX + m * kChunk * 2 + lane * 2));
+            }
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                if (m < M) {   // warp-uniform
+                    const uint32_t emax = __reduce_max_sync(0xffffffffu, (static_cast<uint32_t>(xb[m]) >> 7) & 0xFFu);
+                    const int sh = mx::x_shift(emax);
+                    const uint32_t addr = base + St::kX + m * kChunk * 2 + lane * 2;
+                    asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(mx::x_to_f16(xb[m], sh)) : "memory");
+                    if (lane == 0)
+                        asm volatile("st.shared.f32 [%0], %1;" ::"r"(base + St::kZ + 4 * m), "f"(mx::x_unshift(sh))
+                                     : "memory");
+                }
+            }
+            __syncwarp();
+        };
+
         auto compute = [&](int st, int c) {
             const uint32_t base = ring + st * St::kBytes;
-            if constexpr (kMx) {
-                // lane l rescales x[m][l] of every row m < M; the rows' factors 2^-c go
-                // to the stage's zero-point block, unused without zero-points
-                uint16_t xb[MT];
-#pragma unroll
-                for (int m = 0; m < MT; ++m) {
-                    xb[m] = 0;
-                    if (m < M)
-                        asm volatile("ld.shared.u16 %0, [%1];" : "=h"(xb[m]) : "r"(base + St::kX + m * kChunk * 2 + lane * 2));
-                }
-#pragma unroll
-                for (int m = 0; m < MT; ++m) {
-                    const uint32_t emax = __reduce_max_sync(0xffffffffu, (static_cast<uint32_t>(xb[m]) >> 7) & 0xFFu);
-                    if (m < M) {
-                        const int sh = mx::x_shift(emax);
-                        const uint32_t addr = base + St::kX + m * kChunk * 2 + lane * 2;
-                        asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(mx::x_to_f16(xb[m], sh)) : "memory");
-                        if (lane == 0)
-                            asm volatile("st.shared.f32 [%0], %1;" ::"r"(base + St::kZ + 4 * m), "f"(mx::x_unshift(sh))
-                                         : "memory");
-                    }
-                }
-                __syncwarp();
-            }
+            if constexpr (kMx) mx_rescale(base);
             // scales and zero-points of the lane's columns
             // zw: the zero-point word of the group's first column; zw2: of its last
             // (a 3-column group can cross a word)
@@ -662,15 +665,30 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
             constexpr int NT = MT / 8, SU = CB / 64;
             const uint32_t base = ring + st * St::kBytes;
             const int r = lane >> 2, tg = lane & 3;
+            if constexpr (kMx) mx_rescale(base);
             uint32_t bx[NT][4];
+            float um[NT][2];   // kMx: the factors of the fragment's rows 8 nt + 2 tg (+1)
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
                 uint32_t xw[4];
                 lds<16>(base + St::kX + (8 * nt + r) * kChunk * 2 + tg * 16, xw);   // rows >= M: zero fill
-                bx[nt][0] = __byte_perm(xw[0], xw[2], 0x5410);   // x[k], x[k + 4]
-                bx[nt][1] = __byte_perm(xw[0], xw[2], 0x7632);   // x[k + 1], x[k + 5]
-                bx[nt][2] = __byte_perm(xw[1], xw[3], 0x5410);   // x[k + 2], x[k + 6]
-                bx[nt][3] = __byte_perm(xw[1], xw[3], 0x7632);   // x[k + 3], x[k + 7]
+                if constexpr (kMx) {
+                    // E2M1 pairs are (k, k + 1): x in its own order
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) bx[nt][i] = xw[i];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int m = 8 * nt + 2 * tg + e;
+                        um[nt][e] = 0.f;   // rows >= M: no factor written (and the fragment is zero)
+                        if (m < M)
+                            asm volatile("ld.shared.f32 %0, [%1];" : "=f"(um[nt][e]) : "r"(base + St::kZ + 4 * m));
+                    }
+                } else {
+                    bx[nt][0] = __byte_perm(xw[0], xw[2], 0x5410);   // x[k], x[k + 4]
+                    bx[nt][1] = __byte_perm(xw[0], xw[2], 0x7632);   // x[k + 1], x[k + 5]
+                    bx[nt][2] = __byte_perm(xw[1], xw[3], 0x5410);   // x[k + 2], x[k + 6]
+                    bx[nt][3] = __byte_perm(xw[1], xw[3], 0x7632);   // x[k + 3], x[k + 7]
+                }
             }
 #pragma unroll
             for (int u = 0; u < SU; ++u) {
@@ -678,10 +696,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
                 uint32_t q_lo[4], q_hi[4], s_lo[2], s_hi[2];
                 lds<16>(base + St::kQ + (tg * CB + c_lo) * 4, q_lo);
                 lds<16>(base + St::kQ + (tg * CB + c_hi) * 4, q_hi);
-                lds<8>(base + St::kS + c_lo * 2, s_lo);
-                lds<8>(base + St::kS + c_hi * 2, s_hi);
+                if constexpr (kMx) {   // 4 exponent bytes each
+                    uint32_t e[1];
+                    lds<4>(base + St::kS + c_lo, e);
+                    s_lo[0] = e[0];
+                    lds<4>(base + St::kS + c_hi, e);
+                    s_hi[0] = e[0];
+                    s_lo[1] = s_hi[1] = 0u;
+                } else {
+                    lds<8>(base + St::kS + c_lo * 2, s_lo);
+                    lds<8>(base + St::kS + c_hi * 2, s_hi);
+                }
                 uint32_t z_lo = 0u, z_hi = 0u;   // the 4 columns' zero-points: nibbles 0..3
-                if constexpr (!kSym) {
+                if constexpr (!kSym && !kMx) {
                     if constexpr (kZBulk) {
                         uint32_t v[1];
                         lds<4>(base + St::kZ + (c_lo >> 3) * 4, v);
@@ -702,18 +729,35 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
                     const uint32_t zh = kSym ? 8u : ((z_hi >> (4 * j)) & 0xFu);
                     const uint32_t zzl = A::kMagic + zl * 0x10001u, zzh = A::kMagic + zh * 0x10001u;
                     uint32_t hl[4], hh[4];
+                    float sl, sh;
+                    if constexpr (kMx) {
+                        // codes -> fp16 pairs (k, k + 1); block scales 2^(e - 127)
+                        mx::e2m1x8_to_f16x2(q_lo[j], hl);
+                        mx::e2m1x8_to_f16x2(q_hi[j], hh);
+                        sl = mx::scale_f32((s_lo[0] >> (8 * j)) & 0xFFu);
+                        sh = mx::scale_f32((s_hi[0] >> (8 * j)) & 0xFFu);
+                    } else {
 #pragma unroll
-                    for (int bb = 0; bb < 4; ++bb) {
-                        hl[bb] = A::sub2(and_or(q_lo[j] >> (4 * bb), 0x000F000Fu, A::kMagic), zzl);
-                        hh[bb] = A::sub2(and_or(q_hi[j] >> (4 * bb), 0x000F000Fu, A::kMagic), zzh);
+                        for (int bb = 0; bb < 4; ++bb) {
+                            hl[bb] = A::sub2(and_or(q_lo[j] >> (4 * bb), 0x000F000Fu, A::kMagic), zzl);
+                            hh[bb] = A::sub2(and_or(q_hi[j] >> (4 * bb), 0x000F000Fu, A::kMagic), zzh);
+                        }
+                        sl = A::to_float(static_cast<uint16_t>(s_lo[j >> 1] >> (16 * (j & 1))));
+                        sh = A::to_float(static_cast<uint16_t>(s_hi[j >> 1] >> (16 * (j & 1))));
                     }
-                    const float sl = A::to_float(static_cast<uint16_t>(s_lo[j >> 1] >> (16 * (j & 1))));
-                    const float sh = A::to_float(static_cast<uint16_t>(s_hi[j >> 1] >> (16 * (j & 1))));
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) {
                         float d[4] = {0.f, 0.f, 0.f, 0.f};
-                        mma_m16n8k16<kBf16>(d, hl[0], hh[0], hl[1], hh[1], bx[nt][0], bx[nt][1]);
-                        mma_m16n8k16<kBf16>(d, hl[2], hh[2], hl[3], hh[3], bx[nt][2], bx[nt][3]);
+                        // MXFP4: fp16 x fp16 (x rescaled); int4: the activation dtype
+                        constexpr bool kMmaBf16 = kBf16 && !kMx;
+                        mma_m16n8k16<kMmaBf16>(d, hl[0], hh[0], hl[1], hh[1], bx[nt][0], bx[nt][1]);
+                        mma_m16n8k16<kMmaBf16>(d, hl[2], hh[2], hl[3], hh[3], bx[nt][2], bx[nt][3]);
+                        if constexpr (kMx) {
+                            d[0] *= um[nt][0];
+                            d[1] *= um[nt][1];
+                            d[2] *= um[nt][0];
+                            d[3] *= um[nt][1];
+                        }
                         float* y = &yacc[0][0] + ((nt * SU + u) * 4 + j) * 4;
                         y[0] = fmaf(sl, d[0], y[0]);
                         y[1] = fmaf(sl, d[1], y[1]);
@@ -975,6 +1019,15 @@ cudaError_t launch_dtype(const GemvArgs& a, const GemvPlan& p, cudaStream_t s) {
 }
 
 cudaError_t launch_mx_rows(const GemvArgs& a, const GemvPlan& p, cudaStream_t s) {
+    if (p.mma) {
+        switch (p.mt) {
+            case 8:
+                return p.cols == 2 ? launch_one<true, 8, 2, true, false, false, true, false, true>(a, p, s)
+                                   : launch_one<true, 8, 4, true, false, false, true, false, true>(a, p, s);
+            case 16: return launch_one<true, 16, 2, true, false, false, true, false, true>(a, p, s);
+            default: return cudaErrorInvalidValue;
+        }
+    }
     switch (p.mt) {
         case 1:
             return p.cols == 9 ? launch_one<true, 1, 9, true, false, false, true>(a, p, s)
@@ -1062,8 +1115,8 @@ int cluster_capacity(const DeviceProps& dp, int size) {
 // `narrow`: the 8-row MMA template with 64-column blocks instead of 128.
 GemvPlan plan_cols(int M, int N, int K, bool fact, const DeviceProps& dp, bool narrow) {
     GemvPlan p;
-    p.mma = fact && M >= kMmaMinM &&
-            (M > kFmaSmallMaxM || static_cast<long long>(N) * K > kFmaSmallMaxWeights);
+    // `fact` marks the int4 layer; MXFP4 weights take the same conversion choice
+    p.mma = M >= kMmaMinM && (M > kFmaSmallMaxM || static_cast<long long>(N) * K > kFmaSmallMaxWeights);
     if (p.mma) {
         p.mt = M <= 8 ? 8 : 16;
         p.cols = M <= 8 && !narrow ? 4 : 2;

@@ -64,24 +64,17 @@ cudaError_t launch_gemv(const void* x, const uint32_t* qw, const void* sc, const
                         int M, int N, int K, int g, bool bf16, const GemvPlan& plan, float* partials,
                         uint32_t* tickets, cudaStream_t s);
 
-// w4a16_mxfp4_gemv hands M >= kGemvTensorMinM rows to the few-row
-// tensor-core kernel when the layer has at least gemv_tensor_min_weights(M)
-// weights: its GEMV converts with FP32 FMAs (8 * M per packed word), so its
-// time grows with the row template (6, 8, 12, 16 rows), while the tensor-core
-// kernel's is flat in M with a floor of about 15 us on small layers.
-// Thresholds from timings of both kernels on 12 layer shapes (2048 x 2048 to
-// 43008 x 5376) with the same FMA conversion on W4A16 weights, e.g. (us,
-// GEMV / tensor-core): M=5: 8192 x 8192 28.7 / 28.6, 14336 x 4096 27.0 /
-// 28.4, 16384 x 5376 37.0 / 33.8; M=8: 8192 x 4096 18.7 / 21.3, 11008 x 4096
-// 26.4 / 23.3; M=12: 4096 x 4096 16.0 / 18.2, 8192 x 4096 31.1 / 21.4; M=16:
-// 4096 x 2048 11.4 / 15.8, 6144 x 2048 19.7 / 16.5. (w4a16_gemv converts 2..16
-// rows with tensor-core MMAs and beats the tensor-core kernel at every M.)
-constexpr int kGemvTensorMinM = 5;
-inline long long gemv_tensor_min_weights(long long M) {
-    return M <= 6 ? 64ll << 20 : M <= 8 ? 36ll << 20 : M <= 12 ? 24ll << 20 : 10ll << 20;
-}
+// w4a16_mxfp4_gemv converts 2..16 rows with tensor-core MMAs like the int4
+// GEMV, but rescales every chunk's x rows to fp16 first; with 16 rows that
+// costs more than the MMAs save on large layers, so 9..16 rows of a layer
+// with at least kMxTensorMinWeights weights go to the few-row tensor-core
+// kernel. Measured (us, GEMV / tensor-core kernel): 43008 x 5376 M=8 59.4 /
+// 77.1, M=12 110.5 / 77.3; 16384 x 5376 M=12 47.1 / 36.0; 8192 x 4096 M=12
+// 19.1 / 21.7, M=16 20.0 / 21.7. (w4a16_gemv hands nothing over.)
+constexpr int kGemvTensorMinM = 9;
+constexpr long long kMxTensorMinWeights = 48ll << 20;
 inline bool mx_gemv_uses_tensor_cores(long long M, long long N, long long K) {
-    return M >= kGemvTensorMinM && N * K >= gemv_tensor_min_weights(M);
+    return M >= kGemvTensorMinM && N * K >= kMxTensorMinWeights;
 }
 
 // Size of the GEMV's built-in scratch array (w4a16_gemv_noalloc).
