@@ -229,7 +229,11 @@ w4a16_status w4a16_gemv_noalloc(const void* x, const int32_t* qweight, const voi
  * ascending CTA order (deterministic). This path needs a workspace of
  * w4a16_workspace_bytes(W4A16_OP_GEMM, M, N, K, g) bytes with the GEMV's
  * ownership and zero-fill rules (W4A16_ERR_WORKSPACE otherwise); after a
- * W4A16_ERR_TIMEOUT reported by w4a16_device_status, zero it again.
+ * W4A16_ERR_TIMEOUT reported by w4a16_device_status, zero it again. It is
+ * launched with programmatic stream serialization like w4a16_gemv: its
+ * prologue (barrier setup, tensor-memory allocation, tensor-map prefetch) may
+ * overlap the end of the preceding kernel on `stream`, and every read and
+ * write of caller memory follows that kernel's completion.
  * Larger M runs the kernel described next and needs no workspace.
  *
  * Clusters of two CTAs (one per SM) own 256 x 256 output tiles of a

@@ -131,6 +131,12 @@ constexpr size_t smem_bytes() {
     return 1024 + Cfg<MP>::kLoadStages * Cfg<MP>::kLoadStageBytes + sizeof(Barriers<MP>);
 }
 
+// Launch with programmatic stream serialization (0: plain launches).
+#ifndef W4A16_SKINNY_PDL
+#define W4A16_SKINNY_PDL 1
+#endif
+constexpr bool kSkinnyPdl = W4A16_SKINNY_PDL != 0;
+
 #ifndef W4A16_SKINNY_SPIN
 #define W4A16_SKINNY_SPIN 64
 #endif
@@ -260,6 +266,13 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_cons
     const long long u_begin = streamk ? unit_start(blockIdx.x, U, G) : blockIdx.x;
     const long long u_end = streamk ? unit_start(blockIdx.x + 1, U, G) : tiles;
 
+    // Programmatic launch: the next kernel of the stream may start its
+    // prologue once every CTA of this grid is past this point. Before the
+    // dependency wait below this grid touches no global memory: it only
+    // initialises barriers, prefetches the tensor maps and allocates tensor
+    // memory (one CTA per SM by shared memory, so it never waits there for a
+    // CTA of the preceding grid).
+    if (kSkinnyPdl) griddep_launch_dependents();
     if (threadIdx.x == 0) {
         for (int s = 0; s < L; ++s) {
             mbar_init(smem_u32(&bars->lfull[s]), 1);
@@ -286,6 +299,9 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_cons
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = bars->tmem_base;
+    // every read of x, weights and workspace and every write comes after the
+    // preceding kernel has completed and its writes are visible
+    if (kSkinnyPdl) griddep_wait();
 
     if (warp == 0 || warp == 3) {
         // ------------------------------------------------------------ producer warps
@@ -616,9 +632,18 @@ cudaError_t launch_mp(const void* x, const uint32_t* qw, const void* sc, const u
     const long long units = static_cast<long long>(tiles) * ((K + BK - 1) / BK);
     const bool streamk = M <= kStreamKMaxM;
     const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(streamk ? units : tiles, dp.sms)));
-    kern<<<grid, kThreads, kSmem, s>>>(tx, tw, ts, tz, qz, static_cast<uint16_t*>(y), M, N, K, g, partials, tickets,
-                                       streamk ? 1 : 0, z_tma ? 1 : 0);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = kSkinnyPdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, tx, tw, ts, tz, qz, static_cast<uint16_t*>(y), M, N, K, g, partials, tickets,
+                              streamk ? 1 : 0, z_tma ? 1 : 0);
 }
 
 template <bool kBf16, bool kSym, bool kMx = false>
