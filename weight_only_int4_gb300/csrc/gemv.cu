@@ -1,4 +1,4 @@
-// Decode GEMV of the W4A16 layer, 1 <= M <= 16, on CUDA cores.
+// Decode GEMV of the W4A16 layer (and of MXFP4 weights), 1 <= M <= 16.
 //
 // The kernel is memory-bound: per call it must stream K*N/2 bytes of packed
 // weights, (K/g)*N scales and (K/g)*N/2 bytes of packed zero-points, each once.
@@ -13,7 +13,8 @@
 //     contiguous ranges of items ("stream-K"), so every SM streams the same
 //     number of bytes whatever N and K are. When CTAs have few chunks per
 //     warp, a grid of a whole number of CTAs per column block is taken
-//     instead if it is cheaper: no range then crosses a block boundary.
+//     instead if it is cheaper: no range then crosses a block boundary. One
+//     row takes 288-column blocks where that gives every CTA one whole block.
 //   * Inside a CTA the warps take the chunks of the current column block in
 //     turn. Each warp streams its chunks through its own kStages-deep ring in
 //     shared memory: one lane issues bulk asynchronous copies (TMA, completion
@@ -21,24 +22,28 @@
 //     rows, its scales, its packed zero-points and the x slice, kStages chunks
 //     ahead of the one being converted, so memory and ALU overlap with about
 //     kWarps * (kStages - 1) chunks in flight per CTA and no load instructions
-//     on the lanes. A lane owns COLS columns in groups of 4 adjacent columns,
-//     32 groups apart, so all its shared-memory reads are bank-conflict free.
+//     on the lanes. A lane owns COLS columns in groups of adjacent columns,
+//     32 groups apart, so its shared-memory reads are contiguous across the warp.
 //   * Nibbles become 16-bit floats by the exponent-bias trick: OR a nibble into
-//     the mantissa of 1024.0 (fp16) or 128.0 (bf16). For M <= 4 the zero-point
-//     is applied once per chunk through
+//     the mantissa of 1024.0 (fp16) or 128.0 (bf16). One row (and two rows of
+//     small layers) use FP32 FMAs with the zero-point applied once per chunk
+//     through
 //         sum_k (q - z) x = sum_k (magic + q) x - (magic + z) sum_k x,
 //     with sum_k x of the chunk formed by a warp reduction over the chunk's x
 //     slice (one value per lane) when the chunk is converted, or, when every
 //     warp has many chunks to amortise it over, computed for all chunks once
 //     per CTA after the dependency wait (kXPre); the products
 //     (magic + q) * x are exact in an FP32 FMA with 16-bit inputs
-//     (fma.rn.f32.f16 / .bf16). For M > 4 the zero-point is subtracted from
-//     each nibble pair in packed 16-bit arithmetic (exact) before the FMA. The
-//     scale is applied in FP32 once per chunk.
-//   * Column blocks split between CTAs are finished by the last CTA to arrive
-//     (an atomic ticket per column block): it sums the partial vectors of all
-//     contributing CTAs in ascending CTA order, so the result is deterministic,
-//     and resets the ticket to zero for the next call.
+//     (fma.rn.f32.f16 / .bf16). More rows go through warp-level m16n8k16
+//     tensor-core MMAs (kMma): (q - z) exact in packed 16-bit arithmetic as
+//     the A operand, x as B, FP32 accumulators. The scale is applied in FP32
+//     once per chunk.
+//   * Column blocks split between CTAs are summed deterministically in
+//     ascending CTA order: within a thread-block cluster over distributed
+//     shared memory when the grid is block-aligned and all clusters fit,
+//     otherwise by the last CTA to take the block's atomic ticket, which
+//     reads the others' partial vectors from the workspace and resets the
+//     ticket to zero for the next call.
 #include "internal.h"
 #include "mxfp4.cuh"
 #include "ptx.cuh"
