@@ -70,10 +70,16 @@ namespace {
 #define W4A16_GEMV_STAGES 2
 #endif
 // Chunks per warp whose weights are prefetched into L2 before the grid
-// dependency wait, and whether launches allow programmatic overlap with the
-// preceding kernel of the stream.
+// dependency wait (FMA and MMA conversions), and whether launches allow
+// programmatic overlap with the preceding kernel of the stream. Measured (us,
+// depth 0 / 1 / 2): 1x43008x5376 25.84 / 24.42 / 24.66, 1x5376x21504 15.03 /
+// 14.40 / 14.71 on FMAs; 4x43008x5376 38.75 / 40.21 / 40.18, 4x4096x2048 4.90
+// / 5.03 / 5.15 on MMAs.
 #ifndef W4A16_GEMV_L2_PREFETCH
-#define W4A16_GEMV_L2_PREFETCH 2
+#define W4A16_GEMV_L2_PREFETCH 1
+#endif
+#ifndef W4A16_GEMV_L2_PREFETCH_MMA
+#define W4A16_GEMV_L2_PREFETCH_MMA 0
 #endif
 #ifndef W4A16_GEMV_PDL
 #define W4A16_GEMV_PDL 1
@@ -93,6 +99,7 @@ __host__ __device__ constexpr int ring_stages(bool mma, int mt) {
     return !mma ? kStages : mt == 8 ? W4A16_GEMV_MMA_STAGES8 : W4A16_GEMV_MMA_STAGES16;
 }
 constexpr int kL2Prefetch = W4A16_GEMV_L2_PREFETCH;
+constexpr int kL2PrefetchMma = W4A16_GEMV_L2_PREFETCH_MMA;
 constexpr int kThreads = kWarps * 32;
 constexpr int kChunk = 32;            // rows of K per chunk
 constexpr int kRowsPerChunk = 4;      // packed word rows per chunk
@@ -347,7 +354,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
             const int cb = static_cast<int>(i_begin / chunks);
             const int c0 = static_cast<int>(i_begin - static_cast<long long>(cb) * chunks);
             const int c1 = static_cast<int>(std::min<long long>(chunks, c0 + (i_end - i_begin)));
-            for (int j = 0, c = c0 + warp; j < kL2Prefetch && c < c1; ++j, c += kWarps) {
+            constexpr int kPf = kMma ? kL2PrefetchMma : kL2Prefetch;
+            for (int j = 0, c = c0 + warp; j < kPf && c < c1; ++j, c += kWarps) {
                 const int t = (c * kChunk) >> g_shift;
 #pragma unroll
                 for (int gi = 0; gi < (St::kSplit ? G : 1); ++gi) {
