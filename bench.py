@@ -18,6 +18,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import math
 import os
@@ -47,9 +48,18 @@ KERNEL_SOURCES = {
 }
 
 
+def code_hash(text: str) -> str:
+    """sha256[:16] of a CUDA source with its comments and blank lines removed:
+    edits to comments do not invalidate counters taken on the same code."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    code = "\n".join(line.rstrip() for line in text.split("\n") if line.strip())
+    return hashlib.sha256(code.encode()).hexdigest()[:16]
+
+
 def kernel_hash(kind: str) -> str:
-    with open(KERNEL_SOURCES[kind], "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    with open(KERNEL_SOURCES[kind], encoding="utf-8") as f:
+        return code_hash(f.read())
 
 
 def load_peaks():

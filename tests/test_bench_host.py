@@ -75,3 +75,14 @@ def test_reference_arm_prints_on_rank_zero_only():
     line = json.loads(lines[0][-1])
     assert line["impl"] == "reference"
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_code_hash_ignores_comments_only():
+    """The traffic table keys counters by the kernel's code: comment edits keep
+    the key, any change to the code changes it."""
+    import bench
+    src = "// header\n__global__ void k(int* p) {\n    p[0] = 1;   // store\n}\n/* block\n comment */\n"
+    same = "__global__ void k(int* p) {\n\n    p[0] = 1;\n}\n// another note\n"
+    changed = "__global__ void k(int* p) {\n    p[0] = 2;\n}\n"
+    assert bench.code_hash(src) == bench.code_hash(same)
+    assert bench.code_hash(src) != bench.code_hash(changed)

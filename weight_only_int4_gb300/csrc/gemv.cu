@@ -150,9 +150,11 @@ struct Act<true> {
 // One stage of a warp's ring holds, for one 32-row chunk of K and one column
 // block of CB = 32 * COLS columns: the 4 packed word rows [4][CB], the scales
 // [CB], the zero-point words [CB / 8] and the x slice [M][32]. A lane owns
-// COLS columns in groups of W = min(COLS, 4) adjacent columns, one group per
-// 32*W columns, so every lane-wise shared-memory read of a warp covers
-// contiguous bytes (no bank conflicts).
+// COLS columns in groups of W adjacent columns (W = 4, or 3 for 9 columns a
+// lane), one group per 32*W columns, so every lane-wise shared-memory read of
+// a warp covers contiguous bytes (3-column groups: three 4-byte reads, still
+// conflict free; their 2-byte scale reads conflict a little). The MMA
+// conversion reads the same layout with its own lane mapping.
 __host__ __device__ constexpr int round128(int v) { return (v + 127) & ~127; }
 
 __host__ __device__ constexpr int group_width(int cols) { return cols < 4 ? cols : cols % 4 == 0 ? 4 : 3; }
